@@ -1,0 +1,59 @@
+// rowsum(dO * O): the one quantity of the backward pass that is computed
+// once, outside both gradient kernels ("Flash Attention on a TPU, Line by
+// Line", section "What does the TPU flash attention kernel save for the
+// backward pass?").  Dsum[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d] in fp32.
+//
+// HBM-bound: it reads 4*D bytes per row and writes 4.  Each row is split
+// over D/8 lanes that load 16 bytes of dO and 16 of O (coalesced, one
+// 128-byte line per 8 lanes), multiply in fp32 and reduce with shuffles.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsa {
+namespace {
+
+template <int D>
+__global__ void __launch_bounds__(256) rowsum_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ out,
+                                                     float* __restrict__ dsum, int64_t n_rows) {
+  constexpr int kLanesPerRow = D / 8;  // 16 bytes (8 bf16) per lane
+  constexpr int kRowsPerCta = 256 / kLanesPerRow;
+  const int sub = threadIdx.x % kLanesPerRow;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + threadIdx.x / kLanesPerRow; row < n_rows;
+       row += static_cast<int64_t>(gridDim.x) * kRowsPerCta) {
+    const uint4 a = __ldcs(dout + row * kLanesPerRow + sub);
+    const uint4 b = __ldcs(out + row * kLanesPerRow + sub);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = __bfloat1622float2(a2[e]);
+      const float2 fb = __bfloat1622float2(b2[e]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+#pragma unroll
+    for (int o = kLanesPerRow / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, kLanesPerRow);
+    if (sub == 0) dsum[row] = acc;
+  }
+}
+
+}  // namespace
+
+bsa_status rowsum_launch(const bsa_bwd_args* a, cudaStream_t stream) {
+  const int64_t n_rows = static_cast<int64_t>(a->B) * a->Hq * a->S_q;
+  const int rows_per_cta = 256 / (a->D / 8);
+  const int64_t need = (n_rows + rows_per_cta - 1) / rows_per_cta;
+  const int grid = static_cast<int>(std::min<int64_t>(need, static_cast<int64_t>(num_sms()) * 16));
+  if (a->D == 128)
+    rowsum_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(a->do_), static_cast<const uint4*>(a->o),
+                                                 a->dsum, n_rows);
+  else
+    rowsum_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(a->do_), static_cast<const uint4*>(a->o),
+                                                a->dsum, n_rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "rowsum launch");
+  return BSA_OK;
+}
+
+}  // namespace bsa

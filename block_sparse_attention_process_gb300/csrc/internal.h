@@ -1,0 +1,49 @@
+// Internal declarations shared by the host side of the library.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <string>
+
+#include "../../include/bsa.h"
+
+// Compiled mask, owned by the library.
+struct bsa_mask_info {
+  int32_t kind = 0, orientation = 0, shrink = 1;
+  int32_t heads = 0, rows = 0, cols = 0, width = 0;
+  int64_t q_len = 0, kv_len = 0;
+  int64_t num_partial = 0, n_empty = 0, n_partial = 0, n_full = 0;
+  int32_t data_next_bytes = 1, mask_next_bytes = 0;
+  // mask parameters, kept so the kernels can recompute computable masks
+  int64_t local_left = -1, local_right = -1, chunk = 0;
+  // device storage (one allocation each)
+  int8_t* block_mask = nullptr;      // [heads, rows, width]
+  void* data_next = nullptr;         // [heads, rows, width]
+  void* mask_next = nullptr;         // [heads, rows, width] or null
+  uint8_t* partial = nullptr;        // [num_partial, 128, 128] or null
+  int32_t* q_sequence = nullptr;     // [q_len]
+  int32_t* row_len = nullptr;        // [heads, rows] non-empty blocks per row (internal)
+  int32_t* row_order = nullptr;      // [heads * rows] rows sorted by decreasing row_len (internal)
+};
+
+namespace bsa {
+
+constexpr int kBlock = 128;
+
+void set_last_error(const std::string& msg);
+bsa_status fail(bsa_status s, const std::string& msg);
+bsa_status cuda_fail(cudaError_t e, const char* what);
+uint32_t* device_error_word();          // per-device error word (lazily allocated)
+uint64_t wait_limit_ns();
+
+// Launchers implemented in the .cu files (argument checking is done by the caller).
+bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opts, cudaStream_t stream,
+                             bsa_mask_info** out);
+bsa_status fwd_launch(const bsa_fwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream);
+bsa_status rowsum_launch(const bsa_bwd_args* a, cudaStream_t stream);
+bsa_status dkv_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream);
+bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream);
+bsa_status debug_wait_timeout_launch(cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace bsa

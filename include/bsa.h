@@ -1,0 +1,207 @@
+/*
+ * bsa.h -- C ABI of a GB300 (sm_103a) block-sparse ("splash") attention library.
+ *
+ * The method: "Splash Attention: When the Mask Stops Being Arithmetic and
+ * Becomes the Loop" (explainers.rudrite.com/splash-attention).  A mask is
+ * compiled once into MaskInfo -- one label per block (0 = all zeros, never
+ * computed or fetched; 1 = mixed, computed and masked; 2 = all ones,
+ * computed without masking), the next non-empty key/value block per grid
+ * position (data_next), a deduplicated stack of the mixed blocks of a dense
+ * mask (partial_mask_blocks, pointed at by mask_next), the query indices
+ * (q_sequence) -- and the attention kernels take their loop structure from
+ * it.  The backward pass follows "Flash Attention on a TPU, Line by Line"
+ * (explainers.rudrite.com/pallas-flash-attention-tpu): rowsum(dO*O) is
+ * computed once by its own kernel, then one launch produces dK/dV (queries
+ * innermost) and another dQ (keys innermost), both rebuilding the scores
+ * from Q, K and the saved per-row logsumexp.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Tensors are contiguous BHSD: Q, O, dO, dQ are [B, Hq, S_q, D];
+ *   K, V, dK, dV are [B, Hkv, S_kv, D]; LSE and Dsum are [B, Hq, S_q] fp32.
+ *   Q/K/V/O/dO are bf16.  Query head h reads key/value head
+ *   h / (Hq / Hkv) (contiguous groups: MHA, GQA and MQA).
+ * - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *   aligned.  The library never frees them.
+ * - Blocks are 128 x 128; S_q and S_kv must be multiples of 128; D is 64 or
+ *   128.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *   is asynchronous on that stream except bsa_mask_compile (which
+ *   synchronises once to learn the grid width and the stack size),
+ *   bsa_mask_info_destroy and bsa_get_device_error.
+ * - Calls return a status; none throws.  On failure bsa_last_error()
+ *   returns a message for the calling thread.  Argument errors are found on
+ *   the host before anything is launched.
+ * - Kernels never trap: every device-side wait is bounded; a wait that runs
+ *   out, or an index read from MaskInfo that is out of range, sets a bit in
+ *   the library's device error word and the kernel returns.  Read it with
+ *   bsa_get_device_error.
+ */
+#ifndef BSA_H_
+#define BSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define BSA_API __attribute__((visibility("default")))
+#else
+#define BSA_API
+#endif
+
+typedef void* bsa_stream; /* a cudaStream_t */
+
+typedef enum {
+  BSA_OK = 0,
+  BSA_ERR_INVALID_ARG = 1, /* null pointer, bad shape, S % 128 != 0, Hq % Hkv != 0, wrong MaskInfo */
+  BSA_ERR_UNSUPPORTED = 2, /* D not in {64, 128}, block != 128, S_q != S_kv for a computable mask */
+  BSA_ERR_CUDA = 3,        /* a CUDA runtime call failed (message in bsa_last_error) */
+  BSA_ERR_OOM = 4,         /* the library could not allocate MaskInfo storage */
+  BSA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (device error word) */
+  BSA_ERR_DEVICE = 6       /* a kernel found an out-of-range MaskInfo index (device error word) */
+} bsa_status;
+
+/* Mask kinds ("What is MaskInfo in splash attention?": CausalMask, LocalMask,
+ * ChunkedCausalMask are computable; a dense array is materialised). */
+typedef enum {
+  BSA_MASK_DENSE = 0,          /* dense uint8 0/1 array (nonzero = visible)          */
+  BSA_MASK_CAUSAL = 1,         /* k <= q                                             */
+  BSA_MASK_LOCAL = 2,          /* q - left <= k <= q + right (inclusive; -1 = none)  */
+  BSA_MASK_CHUNKED_CAUSAL = 3, /* q / chunk == k / chunk  and  k <= q               */
+  BSA_MASK_FULL = 4            /* every key visible                                  */
+} bsa_mask_kind;
+
+typedef enum {
+  BSA_ORIENT_FWD = 0, /* rows = query blocks, columns = key blocks (forward and dQ grids) */
+  BSA_ORIENT_DKV = 1  /* rows = key blocks, columns = query blocks (dK/dV grid)           */
+} bsa_orientation;
+
+typedef struct {
+  int32_t kind;          /* bsa_mask_kind */
+  int32_t mask_heads;    /* 1 (shared by every query head) or Hq (one mask per query head) */
+  int64_t q_len, kv_len; /* element sizes of the mask */
+  int64_t local_left;    /* LOCAL: keys back to q - local_left are visible; -1 = unbounded */
+  int64_t local_right;   /* LOCAL: keys up to q + local_right are visible; -1 = unbounded */
+  int64_t chunk;         /* CHUNKED_CAUSAL: chunk length in tokens (> 0) */
+  const uint8_t* dense;  /* DENSE: device [mask_heads, q_len, kv_len] uint8, caller-owned;
+                            only read during bsa_mask_compile */
+} bsa_mask_spec;
+
+typedef struct {
+  int32_t block_q;     /* must be 128 */
+  int32_t block_kv;    /* must be 128 */
+  int32_t shrink;      /* 1: apply the grid-shrink pass; 0: keep the full grid width */
+  int32_t orientation; /* bsa_orientation */
+} bsa_mask_opts;
+
+/* Opaque compiled mask; owned by the library, freed by bsa_mask_info_destroy. */
+typedef struct bsa_mask_info bsa_mask_info;
+
+/* A read-only view of a compiled MaskInfo.  Device pointers stay valid until
+ * bsa_mask_info_destroy.  Integer element sizes are 1, 2 or 4 bytes: each
+ * array takes the smallest signed type its largest value fits in. */
+typedef struct {
+  const int8_t* block_mask;           /* [heads, rows, width] labels 0/1/2 */
+  const void* data_next;              /* [heads, rows, width] key-block (fwd) / query-block (dkv) index */
+  int32_t data_next_bytes;            /* 1, 2 or 4 */
+  const void* mask_next;              /* [heads, rows, width] stack slot; NULL for computable masks */
+  int32_t mask_next_bytes;            /* 1, 2 or 4 (0 if mask_next is NULL) */
+  const uint8_t* partial_mask_blocks; /* [num_partial, 128, 128] 0/1; NULL for computable masks */
+  const int32_t* q_sequence;          /* [q_len] the query indices */
+  int32_t heads, rows, width, cols;   /* width = grid width after shrink; cols = before */
+  int64_t num_partial;                /* P, the stack depth */
+  int64_t n_empty, n_partial, n_full; /* block counts over the unshrunk grid, all heads */
+  int32_t kind, orientation, shrink;
+  int64_t q_len, kv_len;
+} bsa_mask_info_desc;
+
+/* Compile a mask into MaskInfo ("What is MaskInfo in splash attention?",
+ * "What does grid shrinking do in splash attention?").  Runs the classifier,
+ * the partial-block dedup (dense masks only), the next-block pass, the
+ * shrink pass and the integer downcast as kernels on `stream`, then
+ * synchronises `stream` once to size the outputs.  *out receives a new
+ * handle on success and is untouched on failure. */
+BSA_API bsa_status bsa_mask_compile(const bsa_mask_spec* spec, const bsa_mask_opts* opts, bsa_stream stream,
+                            bsa_mask_info** out);
+BSA_API bsa_status bsa_mask_info_view(const bsa_mask_info* info, bsa_mask_info_desc* out);
+/* Frees the handle's device storage (synchronises the device). NULL is accepted. */
+BSA_API bsa_status bsa_mask_info_destroy(bsa_mask_info* info);
+
+typedef struct {
+  const void* q;       /* bf16 [B, Hq, S_q, D] */
+  const void* k;       /* bf16 [B, Hkv, S_kv, D] */
+  const void* v;       /* bf16 [B, Hkv, S_kv, D] */
+  void* o;             /* bf16 [B, Hq, S_q, D], written */
+  float* lse;          /* fp32 [B, Hq, S_q], written: natural-log logsumexp of the scaled
+                          scores of each row (-inf for a row with no visible key) */
+  int32_t B, Hq, Hkv, D;
+  int64_t S_q, S_kv;
+  float softmax_scale; /* NaN selects 1/sqrt(D) */
+} bsa_fwd_args;
+
+/* Block-sparse forward ("What is splash attention and how is it different
+ * from flash attention?"): for every (b, query head, query block) the kernel
+ * walks the MaskInfo row, never fetches or computes label-0 blocks, masks
+ * only label-1 blocks, and runs an online softmax (running max and sum, one
+ * divide at the end).  `fwd_info` must be a BSA_ORIENT_FWD MaskInfo with
+ * q_len == S_q, kv_len == S_kv and mask_heads 1 or Hq.  A query row with no
+ * visible key gets O = 0 and LSE = -inf. */
+BSA_API bsa_status bsa_fwd(const bsa_fwd_args* args, const bsa_mask_info* fwd_info, bsa_stream stream);
+
+typedef struct {
+  const void* q, *k, *v; /* as in bsa_fwd_args */
+  const void* o;         /* bf16 forward output */
+  const float* lse;      /* fp32 forward logsumexp */
+  const void* do_;       /* bf16 [B, Hq, S_q, D] incoming gradient */
+  void* dq;              /* [B, Hq, S_q, D], written; bf16 or fp32 per grad_fp32 */
+  void* dk;              /* [B, Hkv, S_kv, D], written (summed over each query-head group) */
+  void* dv;              /* [B, Hkv, S_kv, D], written (summed over each query-head group) */
+  float* dsum;           /* caller-provided workspace fp32 [B, Hq, S_q]: rowsum(dO*O) */
+  int32_t B, Hq, Hkv, D;
+  int64_t S_q, S_kv;
+  float softmax_scale;   /* NaN selects 1/sqrt(D) */
+  int32_t grad_fp32;     /* 0: dq/dk/dv are bf16; 1: fp32 */
+} bsa_bwd_args;
+
+/* Backward ("Flash Attention on a TPU, Line by Line": "Why does the TPU flash
+ * attention backward pass run two kernels instead of one?", "What does the
+ * TPU flash attention kernel save for the backward pass?").  Runs
+ * bsa_bwd_rowsum, then bsa_bwd_dkv with `dkv_info` (a BSA_ORIENT_DKV
+ * MaskInfo of the same mask), then bsa_bwd_dq with `fwd_info`. */
+BSA_API bsa_status bsa_bwd(const bsa_bwd_args* args, const bsa_mask_info* fwd_info, const bsa_mask_info* dkv_info,
+                   bsa_stream stream);
+/* dsum[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d] (fp32). */
+BSA_API bsa_status bsa_bwd_rowsum(const bsa_bwd_args* args, bsa_stream stream);
+/* dK, dV: grid over (b, kv head, key block), queries innermost. */
+BSA_API bsa_status bsa_bwd_dkv(const bsa_bwd_args* args, const bsa_mask_info* dkv_info, bsa_stream stream);
+/* dQ: grid over (b, query head, query block), keys innermost. */
+BSA_API bsa_status bsa_bwd_dq(const bsa_bwd_args* args, const bsa_mask_info* fwd_info, bsa_stream stream);
+
+/* Synchronises `stream`, returns the device error word in *word (0 = none;
+ * bit 1 = a bounded wait ran out, bit 2 = out-of-range MaskInfo index,
+ * bit 4 = tensor-memory allocation failure) and clears it.  The status is
+ * BSA_ERR_TIMEOUT / BSA_ERR_DEVICE when the word is non-zero. */
+BSA_API bsa_status bsa_get_device_error(bsa_stream stream, uint32_t* word);
+
+/* Time limit of one device-side wait, in nanoseconds (default 2e9).  Applies
+ * to launches made after the call.  0 restores the default. */
+BSA_API bsa_status bsa_set_wait_limit_ns(uint64_t ns);
+
+/* Launches one CTA that waits on an mbarrier nothing ever arrives at, with
+ * the current wait limit, and returns.  Used to check that a wait that runs
+ * out ends with BSA_ERR_TIMEOUT in the device error word instead of a hang. */
+BSA_API bsa_status bsa_debug_wait_timeout(bsa_stream stream);
+
+BSA_API const char* bsa_status_string(bsa_status s);
+BSA_API const char* bsa_last_error(void);
+/* Library version, e.g. "0.1.0". */
+BSA_API const char* bsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BSA_H_ */

@@ -1,0 +1,141 @@
+"""GPU mask compiler vs the oracle: every MaskInfo array bit-exact, same dtypes.
+
+Covers the workloads' masks in both orientations, planted dense masks with
+empty, full and duplicated blocks (several heads, shrink on and off), the
+integer-downcast boundaries, an all-empty mask and determinism.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import lib_mask_args, need_gpu, oracle_mask_args
+from oracle import mask_info as omi
+from workloads import WORKLOADS, bernoulli_mask, planted_block_mask
+
+pytestmark = pytest.mark.gpu
+
+
+def compile_both(kind, q_len, kv_len, *, dense=None, orientation="fwd", shrink=True, okw=None, lkw=None):
+    import block_sparse_attention_process_gb300 as bsa
+    okw = okw or {}
+    lkw = lkw or {}
+    ref = omi.compile_mask_info(kind, q_len, kv_len, dense=dense, orientation=orientation, shrink_grid=shrink,
+                                **okw)
+    dev_dense = None
+    if dense is not None:
+        dev_dense = torch.from_numpy(np.ascontiguousarray(dense)).cuda()
+    info = bsa.mask_compile(kind, q_len, kv_len, dense=dev_dense, orientation=orientation, shrink=shrink, **lkw)
+    got = info.to_host()
+    info.destroy()
+    return ref, got
+
+
+def assert_same(ref, got):
+    assert got["width"] == ref.width
+    assert (got["n_empty"], got["n_partial"], got["n_full"]) == (ref.n_empty, ref.n_partial, ref.n_full)
+    for name in ("block_mask", "data_next"):
+        r, g = getattr(ref, name), got[name]
+        assert g.dtype == r.dtype, (name, g.dtype, r.dtype)
+        assert np.array_equal(g, r), name
+    if ref.mask_next is None:
+        assert got["mask_next"] is None and got["partial_mask_blocks"] is None
+    else:
+        assert got["mask_next"].dtype == ref.mask_next.dtype
+        assert np.array_equal(got["mask_next"], ref.mask_next)
+        assert got["num_partial"] == ref.num_partial_blocks
+        assert np.array_equal(got["partial_mask_blocks"], ref.partial_mask_blocks)
+    assert np.array_equal(got["q_sequence"], ref.q_sequence)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+@pytest.mark.parametrize("orientation", ["fwd", "dkv"])
+def test_workload_masks_bit_exact(name, orientation):
+    need_gpu()
+    w = WORKLOADS[name]
+    dense = None
+    if w.mask.kind == "dense":
+        dense = bernoulli_mask(w.S, w.mask.p, w.mask.seed)
+    ref, got = compile_both(w.mask.kind, w.S, w.S, dense=dense, orientation=orientation,
+                            okw=oracle_mask_args(w.mask, w.S), lkw=lib_mask_args(w.mask))
+    assert_same(ref, got)
+
+
+def test_page_counts_on_gpu():
+    need_gpu()
+    import block_sparse_attention_process_gb300 as bsa
+    c = bsa.mask_compile("causal", 8192, 8192).to_host()
+    assert c["n_empty"] == 2016 and c["width"] == 64
+    loc = bsa.mask_compile("local", 8192, 8192, local_left=1024, local_right=0).to_host()
+    assert loc["width"] == 9
+    dense = torch.from_numpy(bernoulli_mask(2048, 0.1, 1)).cuda()
+    d = bsa.mask_compile("dense", 2048, 2048, dense=dense).to_host()
+    assert d["n_partial"] == 256 and d["partial_mask_blocks"].nbytes == 4 * 1024 * 1024
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+@pytest.mark.parametrize("orientation", ["fwd", "dkv"])
+@pytest.mark.parametrize("shrink", [True, False])
+def test_planted_dense_bit_exact(seed, orientation, shrink):
+    need_gpu()
+    heads, nq, nk = 3, 4, 6
+    m = planted_block_mask(heads, nq, nk, seed=seed)
+    ref, got = compile_both("dense", nq * 128, nk * 128, dense=m, orientation=orientation, shrink=shrink)
+    assert_same(ref, got)
+
+
+@pytest.mark.parametrize("kind,okw,lkw", [
+    ("local", {"left": 200, "right": 70}, {"local_left": 200, "local_right": 70}),
+    ("local", {"left": None, "right": 5}, {"local_left": None, "local_right": 5}),
+    ("local", {"left": 0, "right": 0}, {"local_left": 0, "local_right": 0}),
+    ("chunked", {"chunk": 192}, {"chunk": 192}),
+    ("causal", {}, {}),
+    ("full", {}, {}),
+])
+@pytest.mark.parametrize("orientation", ["fwd", "dkv"])
+@pytest.mark.parametrize("shrink", [True, False])
+def test_computable_masks_bit_exact(kind, okw, lkw, orientation, shrink):
+    need_gpu()
+    ref, got = compile_both(kind, 1152, 1152, orientation=orientation, shrink=shrink, okw=okw, lkw=lkw)
+    assert_same(ref, got)
+
+
+@pytest.mark.parametrize("cols", [128, 129])
+def test_downcast_boundary(cols):
+    need_gpu()
+    dense = np.ones((128, cols * 128), np.uint8)
+    ref, got = compile_both("dense", 128, cols * 128, dense=dense)
+    assert_same(ref, got)
+
+
+def test_mask_next_int16_when_256_partial_blocks():
+    need_gpu()
+    dense = bernoulli_mask(2048, 0.1, 1)
+    ref, got = compile_both("dense", 2048, 2048, dense=dense)
+    assert got["mask_next"].dtype == np.int16
+    assert_same(ref, got)
+
+
+def test_all_empty_mask():
+    need_gpu()
+    dense = np.zeros((256, 384), np.uint8)
+    ref, got = compile_both("dense", 256, 384, dense=dense)
+    assert got["width"] == 0
+    assert_same(ref, got)
+
+
+def test_nonbinary_dense_bytes_are_normalised():
+    need_gpu()
+    rng = np.random.default_rng(5)
+    m = (rng.random((256, 256)) < 0.5).astype(np.uint8) * rng.integers(1, 255, (256, 256)).astype(np.uint8)
+    ref, got = compile_both("dense", 256, 256, dense=m)
+    assert_same(ref, got)
+
+
+def test_compile_is_deterministic():
+    need_gpu()
+    import block_sparse_attention_process_gb300 as bsa
+    dense = torch.from_numpy(planted_block_mask(2, 5, 5, seed=9)).cuda()
+    a = bsa.mask_compile("dense", 640, 640, dense=dense).to_host()
+    b = bsa.mask_compile("dense", 640, 640, dense=dense).to_host()
+    for k in ("block_mask", "data_next", "mask_next", "partial_mask_blocks"):
+        assert np.array_equal(a[k], b[k])
