@@ -1,0 +1,436 @@
+"""Benchmark of the block-sparse attention hot path on GB300.
+
+One step = forward + backward (rowsum, dK/dV launch, dQ launch) of
+block-sparse attention over one batch of synthetic input, with the
+compiled MaskInfo (forward and dK/dV orientations) resident on the device.
+The default workload is GQA 32/8 causal attention at 8192 tokens, D = 128
+(2016 of 4096 blocks skipped per head).
+
+Metric: TFLOP/s over executed blocks.  Forward counts 4*128*128*D FLOP per
+executed (label 1 or 2) block and query head; backward counts 2.5x the
+forward (five GEMMs: one score recompute, dP, dV, dK, dQ); label-0 blocks
+count nothing.  The JSON line also carries the roofline of the dominant
+kernel, the oracle timed on the host cores, an end-to-end number through
+the public API with host buffers, and clocks sampled during the timed
+region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, bernoulli_mask, qkvdo  # noqa: E402
+
+METRIC = "splash fwd/bwd TFLOP/s over executed blocks; % of GB300 bf16 tensor peak"
+DEFAULT_WORKLOAD = "gqa_causal_s8192"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def mask_kwargs(w):
+    if w.mask.kind == "local":
+        return {"local_left": w.mask.left, "local_right": w.mask.right}
+    if w.mask.kind == "chunked":
+        return {"chunk": w.mask.chunk}
+    return {}
+
+
+def flops(w, n_exec_per_head):
+    fwd = n_exec_per_head * w.B * w.Hq * 4 * 128 * 128 * w.D
+    return fwd, 2.5 * fwd
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+        self.file.flush()
+
+    def summary(self):
+        self.file.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_gpu(args):
+    import block_sparse_attention_process_gb300 as bsa
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    pk = peaks()
+
+    # ---------------------------------------------------------------- inputs (resident in HBM)
+    q, k, v, do = qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed + rank)
+    dense_h = bernoulli_mask(w.S, w.mask.p, w.mask.seed) if w.mask.kind == "dense" else None
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    dense_d = None if dense_h is None else torch.from_numpy(dense_h).to(dev)
+
+    t0 = time.perf_counter()
+    info = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dense_d, **mask_kwargs(w))
+    dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dense_d, orientation="dkv", **mask_kwargs(w))
+    torch.cuda.synchronize()
+    compile_ms = (time.perf_counter() - t0) * 1e3
+    d = info.desc()
+    n_exec = (d.n_partial + d.n_full) // d.heads
+    f_fwd, f_bwd = flops(w, n_exec)
+
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(qd)
+    dk = torch.empty_like(kd)
+    dv = torch.empty_like(vd)
+    dsum = torch.empty_like(lse)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    n_ev = 5
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        bsa.fwd(qd, kd, vd, info, o=o, lse=lse)
+        if evs is not None:
+            evs[1].record(stream)
+        bsa.bwd_rowsum(o, dod, dsum=dsum)
+        if evs is not None:
+            evs[2].record(stream)
+        bsa.bwd_dkv(qd, kd, vd, o, lse, dod, dsum, dkv, dk=dk, dv=dv)
+        if evs is not None:
+            evs[3].record(stream)
+        bsa.bwd_dq(qd, kd, vd, o, lse, dod, dsum, info, dq=dq)
+        if evs is not None:
+            evs[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    assert bsa.get_device_error() == 0
+
+    # ---------------------------------------------------------------- timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()          # L2 flush between steps (outside the events)
+            step(evs[i])
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    assert bsa.get_device_error() == 0
+    per = {"fwd": [], "rowsum": [], "dkv": [], "dq": [], "step": []}
+    for e in evs:
+        per["fwd"].append(e[0].elapsed_time(e[1]))
+        per["rowsum"].append(e[1].elapsed_time(e[2]))
+        per["dkv"].append(e[2].elapsed_time(e[3]))
+        per["dq"].append(e[3].elapsed_time(e[4]))
+        per["step"].append(e[0].elapsed_time(e[4]))
+    ms = {k: sum(v) / len(v) for k, v in per.items()}
+    step_ms = ms["step"]
+    if ws > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = ws * (f_fwd + f_bwd) / (step_ms * 1e-3) / 1e12
+
+    # per-kernel algorithmic work: executed GEMMs of 2*128*128*D FLOP per block and q head
+    gemm = n_exec * w.B * w.Hq * 2 * 128 * 128 * w.D
+    kern = {
+        "fwd": {"flop": 2 * gemm, "ms": ms["fwd"]},
+        "dkv": {"flop": 4 * gemm, "ms": ms["dkv"]},
+        "dq": {"flop": 3 * gemm, "ms": ms["dq"]},
+    }
+    rowsum_bytes = 4 * w.B * w.Hq * w.S * w.D + 4 * w.B * w.Hq * w.S
+    dom = max(kern, key=lambda k: kern[k]["ms"])
+    achieved = kern[dom]["flop"] / (kern[dom]["ms"] * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        ent = tj.get(args.workload, {}).get(dom)
+        if ent and ent.get("valid", False):
+            traffic = ent["bytes_per_launch"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
+                "peak_source": f"{pk['source']} bf16 burst"}
+
+    # ---------------------------------------------------------------- end to end through the public API
+    e2e = run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, f_fwd + f_bwd, ws)
+
+    out = None
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline or ws > 1 else cpu_baseline(w, dense_h, n_exec, seconds=args.cpu_seconds)
+        out = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 Q/K/V/dO; no dataset)",
+            "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D,
+                       "mask": w.mask.kind, "block": 128, "executed_blocks_per_head": n_exec,
+                       "l2": "flushed between steps (512 MiB write, outside the timed events)",
+                       "parallelism": f"replicas x{ws} (independent batches, no collective)"},
+            "frac_of_peak": round(value / pk["bf16_tflops"], 4),
+            "kernels_ms": {k: round(v, 4) for k, v in ms.items()},
+            "kernels_tflops": {k: round(kern[k]["flop"] / (kern[k]["ms"] * 1e-3) / 1e12, 1) for k in kern},
+            "fwd_tflops": round(f_fwd / (ms["fwd"] * 1e-3) / 1e12, 1),
+            "bwd_tflops": round(f_bwd / ((ms["rowsum"] + ms["dkv"] + ms["dq"]) * 1e-3) / 1e12, 1),
+            "rowsum_gbs": round(rowsum_bytes / (ms["rowsum"] * 1e-3) / 1e9, 1),
+            "mask_compile_ms": round(compile_ms, 3),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return out
+
+
+def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws):
+    """Same metric through the public API from pinned host buffers: H2D of the
+    step's inputs, mask compile, forward, backward, D2H of the gradients."""
+    qh, kh, vh, doh = (t.pin_memory() for t in (q, k, v, do))
+    dense_hp = None if dense_h is None else torch.from_numpy(dense_h).pin_memory()
+    outs_h = [torch.empty(q.shape, dtype=torch.bfloat16).pin_memory(),
+              torch.empty(k.shape, dtype=torch.bfloat16).pin_memory(),
+              torch.empty(v.shape, dtype=torch.bfloat16).pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, doh))
+    if dense_hp is not None:
+        h2d += dense_hp.numel()
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+
+    def one():
+        qd, kd, vd, dod = (t.to(dev, non_blocking=True) for t in (qh, kh, vh, doh))
+        dd = None if dense_hp is None else dense_hp.to(dev, non_blocking=True)
+        info = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, **mask_kwargs(w))
+        dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, orientation="dkv", **mask_kwargs(w))
+        o, lse = bsa.fwd(qd, kd, vd, info)
+        dq, dk, dv = bsa.bwd(qd, kd, vd, o, lse, dod, info, dkv)
+        for hst, dvc in zip(outs_h, (dq, dk, dv)):
+            hst.copy_(dvc, non_blocking=True)
+        torch.cuda.synchronize()
+        info.destroy()
+        dkv.destroy()
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    n = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        one()
+    dt = (time.perf_counter() - t0) / n
+    if ws > 1:
+        t = torch.tensor([dt], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": round(ws * total_flop / dt / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(dt * 1e3, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "includes": "H2D Q/K/V/dO, mask compile (fwd+dkv), fwd, bwd, D2H dQ/dK/dV"}
+
+
+ORACLE_ROWS = 1024   # query rows per oracle sample (one row chunk of one head)
+
+
+def oracle_setup(w, dense_h):
+    """The oracle's mask (for its attention) and non-empty blocks per block row."""
+    from oracle import mask_info as omi
+    mask = {"kind": w.mask.kind, "kv_len": w.S}
+    kw = {}
+    if w.mask.kind == "local":
+        kw = dict(left=w.mask.left, right=w.mask.right)
+    elif w.mask.kind == "chunked":
+        kw = dict(chunk=w.mask.chunk)
+    elif w.mask.kind == "dense":
+        mask.update(dense=dense_h)
+    mask.update(kw)
+    info = omi.compile_mask_info(w.mask.kind, w.S, w.S, dense=dense_h, **kw)
+    per_row = (info.labels_unshrunk[0] != 0).sum(axis=1)
+    return mask, per_row
+
+
+def oracle_sample_step(w, inputs, mask, per_row, b, h, chunk):
+    """The oracle's forward + backward for query rows [chunk*1024, +1024) of one
+    (batch, q head): scores against every key, P, O, Dsum, dP, dS, dQ and that
+    chunk's contributions to dK/dV.  Returns (seconds, executed-block FLOP)."""
+    from oracle import attention as oatt
+    q, k, v, do = inputs
+    g = h // (w.Hq // w.Hkv)
+    r0 = chunk * ORACLE_ROWS
+    r1 = min(w.S, r0 + ORACLE_ROWS)
+    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    base = oatt.mask_rows_for(mask, 0)
+    rows_fn = lambda r: base(np.asarray(r) + r0)  # noqa: E731
+    args = (f(q[b, h, r0:r1]), f(k[b, g]), f(v[b, g]), f(do[b, h, r0:r1]))
+    t0 = time.perf_counter()
+    oatt.head_backward(*args, rows_fn, 1 / math.sqrt(w.D))
+    dt = time.perf_counter() - t0
+    blocks = int(per_row[r0 // 128:r1 // 128].sum())
+    return dt, 3.5 * blocks * 4 * 128 * 128 * w.D
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def cpu_baseline(w, dense_h, n_exec, seconds=20.0):
+    """The oracle (as it stands) on the host cores, on a bounded sample: 1024-row
+    chunks of (batch, q head) slices of the workload, forward + backward, for
+    about `seconds` of CPU work; reported in the same unit (TFLOP/s counted
+    over the executed blocks of the rows processed)."""
+    inputs = qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed)
+    mask, per_row = oracle_setup(w, dense_h)
+    n_chunks = max(1, w.S // ORACLE_ROWS)
+    spent, fl, n = 0.0, 0.0, 0
+    while spent < seconds and n < w.B * w.Hq * n_chunks:
+        dt, f = oracle_sample_step(w, inputs, mask, per_row, (n // n_chunks) % w.B, (n // n_chunks) % w.Hq,
+                                   n % n_chunks)
+        spent += dt
+        fl += f
+        n += 1
+    return {"value": round(fl / spent / 1e12, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} chunks of 1024 query rows (of {w.B * w.Hq * n_chunks}), fp64 fwd+bwd, {spent:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle timed on the host cores, same metric/config.
+    Each step is a bounded sample of the workload: one 1024-row chunk of one
+    (batch, q head), forward + backward."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    dense_h = bernoulli_mask(w.S, w.mask.p, w.mask.seed) if w.mask.kind == "dense" else None
+    inputs = qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed)
+    mask, per_row = oracle_setup(w, dense_h)
+    n_chunks = max(1, w.S // ORACLE_ROWS)
+    for i in range(args.warmup):
+        oracle_sample_step(w, inputs, mask, per_row, 0, i % w.Hq, i % n_chunks)
+    spent, fl = 0.0, 0.0
+    for i in range(args.steps):
+        dt, f = oracle_sample_step(w, inputs, mask, per_row, i % w.B, i % w.Hq, i % n_chunks)
+        spent += dt
+        fl += f
+    value = fl / spent / 1e12
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(spent / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16-rounded inputs)",
+        "config": {"workload": args.workload, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D,
+                   "mask": w.mask.kind},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": "each step: one 1024-row chunk of one (batch, q-head) slice, fp64 fwd+bwd"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

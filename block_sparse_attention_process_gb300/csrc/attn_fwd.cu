@@ -439,25 +439,7 @@ bsa_status launch_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, float sc
   p.scale_log2 = scale * 1.4426950408889634f;
   p.o = static_cast<__nv_bfloat16*>(a->o);
   p.lse = a->lse;
-  p.mi.block_mask = info->block_mask;
-  p.mi.data_next = info->data_next;
-  p.mi.mask_next = info->mask_next;
-  p.mi.partial = info->partial;
-  p.mi.q_sequence = info->q_sequence;
-  p.mi.row_len = info->row_len;
-  p.mi.row_order = info->row_order;
-  p.mi.heads = info->heads;
-  p.mi.rows = info->rows;
-  p.mi.width = info->width;
-  p.mi.cols = info->cols;
-  p.mi.dn_bytes = info->data_next_bytes;
-  p.mi.mn_bytes = info->mask_next_bytes;
-  p.mi.kind = info->kind;
-  p.mi.orientation = info->orientation;
-  p.mi.num_partial = info->num_partial;
-  p.mi.left = info->local_left;
-  p.mi.right = info->local_right;
-  p.mi.chunk = info->chunk;
+  p.mi = mask_info_dev(info);
   p.n_tiles = a->B * a->Hq * p.nQ;
   p.err = device_error_word();
   p.wait_ns = wait_limit_ns();

@@ -4,6 +4,7 @@
 #include <cstdint>
 
 #include "../../include/bsa.h"
+#include "internal.h"
 #include "ptx.cuh"
 
 namespace bsa {
@@ -22,6 +23,30 @@ struct MaskInfoDev {
   int64_t num_partial;
   int64_t left, right, chunk;
 };
+
+inline MaskInfoDev mask_info_dev(const bsa_mask_info* info) {
+  MaskInfoDev m{};
+  m.block_mask = info->block_mask;
+  m.data_next = info->data_next;
+  m.mask_next = info->mask_next;
+  m.partial = info->partial;
+  m.q_sequence = info->q_sequence;
+  m.row_len = info->row_len;
+  m.row_order = info->row_order;
+  m.heads = info->heads;
+  m.rows = info->rows;
+  m.width = info->width;
+  m.cols = info->cols;
+  m.dn_bytes = info->data_next_bytes;
+  m.mn_bytes = info->mask_next_bytes;
+  m.kind = info->kind;
+  m.orientation = info->orientation;
+  m.num_partial = info->num_partial;
+  m.left = info->local_left;
+  m.right = info->local_right;
+  m.chunk = info->chunk;
+  return m;
+}
 
 __device__ __forceinline__ int32_t load_idx(const void* base, int bytes, int64_t i) {
   if (bytes == 1) return static_cast<const int8_t*>(base)[i];
