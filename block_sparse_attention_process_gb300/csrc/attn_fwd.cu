@@ -12,14 +12,19 @@
 // normaliser, a rescale of the accumulator when the maximum moves, and one
 // divide at the end.
 //
-// GB300 design (one CTA per SM, persistent):
-//   warp 0      TMA producer: Q tile (2 buffers), K and V blocks (2-stage rings)
-//   warp 1      tcgen05 issuer: S = Q K^T into TMEM (2 buffers), O += P V
-//               with P read from TMEM (aliases its S buffer as bf16)
-//   warps 4-7   softmax (one query row per thread): mask, row max, exp2,
+// GB300 design (one persistent CTA per SM, warp-specialised):
+//   warp 0      TMA producer of Q tiles (2 buffers) and K blocks (3 stages)
+//   warp 1      tcgen05 issuer, warp-converged (one elected lane issues):
+//               S = Q K^T into one of three TMEM score buffers, up to three
+//               blocks ahead of the P V it is waiting for, and O += P V
+//               with P read from TMEM (bf16 over its score buffer)
+//   warp 2      TMA producer of V blocks (2 stages)
+//   warps 4-7   softmax, one query row per thread: mask, row max, exp2,
 //               row sum, P to TMEM, lazy O rescale in TMEM, epilogue
-// Work tiles are (batch, query head, query block), visited longest row
-// first; consecutive tiles take consecutive heads of a KV group so
+// Each CTA walks one fixed sequence of (tile, block) pairs; every role
+// walks it the same way, so the pipelines stay in step without sharing
+// state.  Work tiles are (batch, query head, query block), longest rows
+// first; consecutive tiles take consecutive heads of a KV group so that
 // concurrently running CTAs share K/V blocks through L2.
 #include <cmath>
 
@@ -31,12 +36,14 @@
 namespace bsa {
 namespace {
 
-constexpr int kStagesK = 2;
+constexpr int kStagesK = 3;
+static_assert(kStagesK == 3, "the K stage of block n is released by the S buffer barrier of block n");
 constexpr int kStagesV = 2;
+constexpr int kSBufs = 3;         // score buffers in TMEM (== K stages: S complete frees its K stage)
+constexpr int kInfoRing = 16;     // block descriptors published by the K producer
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;    // two S/P buffers at columns 0 and 128
-constexpr uint32_t kTmemO = 256;  // O accumulator
+constexpr uint32_t kTmemO = 384;  // O accumulator after three 128-column score buffers
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by more
 
 template <int D>
@@ -46,10 +53,11 @@ struct __align__(1024) FwdSmem {
   uint8_t k[kStagesK][kTileBytes];
   uint8_t v[kStagesV][kTileBytes];
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStagesK], k_empty[kStagesK];
+  uint64_t k_full[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
-  uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, o_full, o_empty, drain;
+  uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
+  uint64_t o_full, o_empty, drain;
+  uint4 binfo[kInfoRing];  // per block: {col | label<<16 | first<<20 | last<<21, slot, tile, 0}
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -92,21 +100,65 @@ __device__ __forceinline__ Tile decode_tile(const FwdParams& p, int32_t T) {
   return t;
 }
 
-// Walks the non-empty positions of one MaskInfo row.  Every role walks the
-// same row the same way, so all of them see the same block sequence.
-struct RowWalk {
-  int32_t pos = 0, taken = 0;
-  __device__ __forceinline__ bool next(const FwdParams& p, const Tile& t, BlockRef& out) {
-    while (taken < t.n && pos < p.mi.width) {
-      const BlockRef r = read_block(p.mi, t.row_base, pos++, p.err);
-      if (r.label != 0) {
-        ++taken;
-        out = r;
-        return true;
+// Cursor over this CTA's (tile, block) sequence.  Tiles without blocks are
+// skipped.  Each tile yields exactly row_len blocks: the non-empty MaskInfo
+// positions in order (a malformed row that runs out early is padded with
+// flagged dummy blocks so that every role still sees the same count).  The
+// entry after the one handed out is loaded ahead of use.
+struct Seq {
+  int32_t T;
+  Tile t;
+  int32_t j;    // blocks of the current tile handed out so far
+  int32_t pos;  // MaskInfo position of the entry loaded ahead
+  RawRef ahead;
+  bool valid;
+
+  __device__ __forceinline__ void start_tile(const FwdParams& p) {
+    while (true) {
+      T += gridDim.x;
+      if (T >= p.n_tiles) {
+        valid = false;
+        return;
+      }
+      t = decode_tile(p, T);
+      if (t.n > 0) break;
+    }
+    j = 0;
+    pos = 0;
+    if (p.mi.width > 0) ahead = load_block(p.mi, t.row_base, 0);
+    valid = true;
+  }
+  __device__ __forceinline__ void init(const FwdParams& p) {
+    T = static_cast<int32_t>(blockIdx.x) - static_cast<int32_t>(gridDim.x);
+    start_tile(p);
+  }
+  // Next block; `first`/`last` mark the tile's first and last block.  After
+  // the last block the caller moves on with finish_tile().
+  __device__ __forceinline__ bool next(const FwdParams& p, BlockRef& br, bool& first, bool& last) {
+    if (!valid) return false;
+    bool found = false;
+    while (pos < p.mi.width) {
+      const RawRef cur = ahead;
+      ++pos;
+      if (pos < p.mi.width) ahead = load_block(p.mi, t.row_base, pos);
+      br = check_block(p.mi, cur, p.err);
+      if (br.label != 0) {
+        found = true;
+        break;
       }
     }
-    return false;
+    if (!found) {  // malformed row: fewer non-empty entries than row_len
+      if (p.err) atomicOr(p.err, DEV_ERR_BOUNDS);
+      br.label = 2;
+      br.col = 0;
+      br.slot = 0;
+    }
+    first = j == 0;
+    ++j;
+    last = j == t.n;
+    return true;
   }
+  __device__ __forceinline__ void finish_tile(const FwdParams& p) { start_tile(p); }
 };
 
 template <int D>
@@ -127,18 +179,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.q_full[i], 1);
       mbar_init(&s.q_empty[i], 1);
+    }
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.pv_done[i], 1);
     }
-    for (int i = 0; i < kStagesK; ++i) {
-      mbar_init(&s.k_full[i], 1);
-      mbar_init(&s.k_empty[i], 1);
-    }
+    for (int i = 0; i < kStagesK; ++i) mbar_init(&s.k_full[i], 1);
     for (int i = 0; i < kStagesV; ++i) {
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_empty[i], 1);
     }
-    mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_full, 1);
     mbar_init(&s.o_empty, 128);
     mbar_init(&s.drain, 1);
@@ -155,41 +206,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      uint32_t q_loads = 0, k_loads = 0, v_loads = 0;
+      uint32_t q_loads = 0, k_loads = 0;
       bool ok = true;
-      for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
-        const Tile t = decode_tile(p, T);
-        if (t.n == 0) continue;
-        const uint32_t qb = q_loads & 1u;
-        if (q_loads >= 2 && !mbar_wait(&s.q_empty[qb], ((q_loads >> 1) - 1) & 1u, wc)) { ok = false; break; }
-        mbar_arrive_expect_tx(&s.q_full[qb], kTileBytes);
-        const int32_t qrow = static_cast<int32_t>((static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + t.i * 128);
-        for (int c = 0; c < kChunks; ++c) tma_load_2d(s.q[qb] + c * 16384, &tm_q, &s.q_full[qb], c * 64, qrow, pol_q);
-        ++q_loads;
-        const int32_t g = t.hq / (p.Hq / p.Hkv);
-        const int64_t kv_base = (static_cast<int64_t>(t.b) * p.Hkv + g) * p.Skv;
-        RowWalk w;
-        BlockRef br;
-        while (w.next(p, t, br)) {
-          const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
-          const uint32_t ks = k_loads % kStagesK;
-          if (k_loads >= kStagesK && !mbar_wait(&s.k_empty[ks], ((k_loads / kStagesK) - 1) & 1u, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.k_full[ks], kTileBytes);
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(s.k[ks] + c * 16384, &tm_k, &s.k_full[ks], c * 64, krow, pol_kv);
-          ++k_loads;
-          const uint32_t vs = v_loads % kStagesV;
-          if (v_loads >= kStagesV && !mbar_wait(&s.v_empty[vs], ((v_loads / kStagesV) - 1) & 1u, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.v_full[vs], kTileBytes);
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(s.v[vs] + c * 16384, &tm_v, &s.v_full[vs], c * 64, krow, pol_kv);
-          ++v_loads;
+      Seq sq;
+      sq.init(p);
+      BlockRef br;
+      bool first, last;
+      int64_t kv_base = 0;
+      while (ok && sq.next(p, br, first, last)) {
+        if (first) {
+          const uint32_t qb = q_loads & 1u;
+          if (q_loads >= 2 && !mbar_wait(&s.q_empty[qb], ((q_loads >> 1) - 1) & 1u, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.q_full[qb], kTileBytes);
+          const int32_t qrow = static_cast<int32_t>((static_cast<int64_t>(sq.t.b) * p.Hq + sq.t.hq) * p.Sq + sq.t.i * 128);
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(s.q[qb] + c * 16384, &tm_q, &s.q_full[qb], c * 64, qrow, pol_q);
+          ++q_loads;
+          kv_base = (static_cast<int64_t>(sq.t.b) * p.Hkv + sq.t.hq / (p.Hq / p.Hkv)) * p.Skv;
         }
+        const uint32_t ks = k_loads % kStagesK;
+        if (k_loads >= kStagesK && !mbar_wait(&s.s_full[ks], ((k_loads / kStagesK) - 1) & 1u, wc)) { ok = false; break; }
+        s.binfo[k_loads % kInfoRing] =
+            make_uint4(static_cast<uint32_t>(br.col) | (static_cast<uint32_t>(br.label) << 16) | (first ? 1u << 20 : 0u) |
+                           (last ? 1u << 21 : 0u),
+                       static_cast<uint32_t>(br.slot), static_cast<uint32_t>(sq.T), 0u);
+        mbar_arrive_expect_tx(&s.k_full[ks], kTileBytes);
+        const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
+        for (int c = 0; c < kChunks; ++c) tma_load_2d(s.k[ks] + c * 16384, &tm_k, &s.k_full[ks], c * 64, krow, pol_kv);
+        ++k_loads;
+        if (last) sq.finish_tile(p);
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
@@ -198,216 +248,301 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t i = (q_loads > 2 ? q_loads - 2 : 0); i < q_loads; ++i) (void)mbar_wait(&s.q_full[i & 1u], (i >> 1) & 1u, dw);
         for (uint32_t i = (k_loads > kStagesK ? k_loads - kStagesK : 0); i < k_loads; ++i)
           (void)mbar_wait(&s.k_full[i % kStagesK], (i / kStagesK) & 1u, dw);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ V producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_kv = policy_evict_last();
+      uint32_t v_loads = 0;
+      bool ok = true;
+      Seq sq;
+      sq.init(p);
+      BlockRef br;
+      bool first, last;
+      int64_t kv_base = 0;
+      while (ok && sq.next(p, br, first, last)) {
+        if (first) kv_base = (static_cast<int64_t>(sq.t.b) * p.Hkv + sq.t.hq / (p.Hq / p.Hkv)) * p.Skv;
+        const uint32_t vs = v_loads % kStagesV;
+        if (v_loads >= kStagesV && !mbar_wait(&s.v_empty[vs], ((v_loads / kStagesV) - 1) & 1u, wc)) { ok = false; break; }
+        mbar_arrive_expect_tx(&s.v_full[vs], kTileBytes);
+        const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
+        for (int c = 0; c < kChunks; ++c) tma_load_2d(s.v[vs] + c * 16384, &tm_v, &s.v_full[vs], c * 64, krow, pol_kv);
+        ++v_loads;
+        if (last) sq.finish_tile(p);
+      }
+      if (!ok) {
+        uint32_t dummy_abort = 0;
+        WaitCtl dw{nullptr, &dummy_abort, p.wait_ns};
         for (uint32_t i = (v_loads > kStagesV ? v_loads - kStagesV : 0); i < v_loads; ++i)
           (void)mbar_wait(&s.v_full[i % kStagesV], (i / kStagesV) & 1u, dw);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
-      uint32_t q_uses = 0, k_uses = 0, v_uses = 0, s_uses = 0, o_uses = 0;
-      bool ok = true;
-      auto issue_pv = [&](uint32_t sidx, bool first) -> bool {
-        const uint32_t pb = sidx & 1u;
-        if (!mbar_wait(&s.p_full[pb], (sidx >> 1) & 1u, wc)) return false;
-        if (first && o_uses > 0 && !mbar_wait(&s.o_empty, (o_uses - 1) & 1u, wc)) return false;
-        const uint32_t vs = v_uses % kStagesV;
-        if (!mbar_wait(&s.v_full[vs], (v_uses / kStagesV) & 1u, wc)) return false;
-        tc_fence_after();
-        const uint32_t vbase = smem_u32(s.v[vs]);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, 16384, 1024);
-          mma_ts(tmem + kTmemO, tmem + kTmemS + pb * 128 + kk * 8, bdesc, idesc_o, (first && kk == 0) ? 0u : 1u);
-        }
-        mma_commit(&s.v_empty[vs]);
-        mma_commit(&s.pv_done);
-        ++v_uses;
-        return true;
-      };
-      for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
-        const Tile t = decode_tile(p, T);
-        if (t.n == 0) continue;
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+    // descriptors of buffer 0; buffers of one kind are contiguous, kTileBytes apart
+    const uint64_t qdesc0 = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
+    const uint64_t kdesc0 = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
+    const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v[0]), 16384, 1024);
+    constexpr uint64_t kTileDesc = kTileBytes >> 4;
+    // Total blocks of this CTA (same count every role walks).
+    uint32_t total = 0;
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(decode_tile(p, T).n);
+    uint32_t s_cnt = 0, pv_cnt = 0, q_uses = 0, o_uses = 0;
+    uint64_t cur_q = qdesc0;
+    bool ok = true;
+
+    auto issue_s = [&]() -> bool {
+      const uint32_t ks = s_cnt % kStagesK;
+      if (!mbar_wait_warp(&s.k_full[ks], (s_cnt / kStagesK) & 1u, wc)) return false;
+      const uint32_t info = s.binfo[s_cnt % kInfoRing].x;
+      if (info & (1u << 20)) {  // first block of a tile: its Q buffer
         const uint32_t qb = q_uses & 1u;
-        if (!mbar_wait(&s.q_full[qb], (q_uses >> 1) & 1u, wc)) { ok = false; break; }
-        const uint32_t qbase = smem_u32(s.q[qb]);
-        uint32_t exec = 0;
-        RowWalk w;
-        BlockRef br;
-        while (w.next(p, t, br)) {
-          const uint32_t ks = k_uses % kStagesK;
-          if (!mbar_wait(&s.k_full[ks], (k_uses / kStagesK) & 1u, wc)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kbase = smem_u32(s.k[ks]);
-          const uint32_t sb = s_uses & 1u;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + kTmemS + sb * 128, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                   idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&s.s_full[sb]);
-          mma_commit(&s.k_empty[ks]);
-          ++k_uses;
-          if (exec > 0 && !issue_pv(s_uses - 1, exec == 1)) { ok = false; break; }
-          ++s_uses;
-          ++exec;
-        }
-        if (!ok) break;
-        mma_commit(&s.q_empty[qb]);
-        ++q_uses;
-        if (exec > 0) {
-          if (!issue_pv(s_uses - 1, exec == 1)) { ok = false; break; }
-          mma_commit(&s.o_full);
-          ++o_uses;
-        }
+        if (!mbar_wait_warp(&s.q_full[qb], (q_uses >> 1) & 1u, wc)) return false;
+        cur_q = qdesc0 + qb * kTileDesc;
       }
-      // Every MMA issued so far completes before tensor memory is released.
-      mma_commit(&s.drain);
-      uint32_t dummy_abort = 0;
-      WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
-      (void)mbar_wait(&s.drain, 0, dw);
+      tc_fence_after();
+      const uint32_t sb = s_cnt % kSBufs;
+      const uint64_t kd = kdesc0 + ks * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+        mma_ss_elect(tmem + sb * 128, cur_q + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(&s.s_full[sb]);  // also frees K stage ks
+      if (info & (1u << 21)) {          // last block of the tile: its Q buffer is free after this S
+        mma_commit_elect(&s.q_empty[q_uses & 1u]);
+        ++q_uses;
+      }
+      ++s_cnt;
+      return true;
+    };
+
+    while (ok && s_cnt < total && s_cnt < static_cast<uint32_t>(kSBufs)) ok = issue_s();
+    while (ok && pv_cnt < total) {
+      const uint32_t info = s.binfo[pv_cnt % kInfoRing].x;
+      const bool pv_first = (info >> 20) & 1u, pv_last = (info >> 21) & 1u;
+      const uint32_t pb = pv_cnt % kSBufs;
+      if (!mbar_wait_warp(&s.p_full[pb], (pv_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
+      if (pv_first && o_uses > 0 && !mbar_wait_warp(&s.o_empty, (o_uses - 1) & 1u, wc)) { ok = false; break; }
+      const uint32_t vs = pv_cnt % kStagesV;
+      if (!mbar_wait_warp(&s.v_full[vs], (pv_cnt / kStagesV) & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t vd = vdesc0 + vs * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_elect(tmem + kTmemO, tmem + pb * 128 + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_o,
+                     (pv_first && kk == 0) ? 0u : 1u);
+      mma_commit_elect(&s.v_empty[vs]);
+      mma_commit_elect(&s.pv_done[pb]);
+      if (pv_last) {
+        mma_commit_elect(&s.o_full);
+        ++o_uses;
+      }
+      ++pv_cnt;
+      // S for the block kSBufs ahead reuses this P buffer: issued after this P V.
+      if (s_cnt < total) ok = issue_s();
     }
+    // Every MMA issued so far completes before tensor memory is released.
+    mma_commit_elect(&s.drain);
+    uint32_t dummy_abort = 0;
+    WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
+    (void)mbar_wait(&s.drain, 0, dw);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int r = static_cast<int>(threadIdx.x) - 128;         // query row in the tile == TMEM lane
+    const int r = static_cast<int>(threadIdx.x) - 128;  // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float scale_log2 = p.scale_log2;
-    uint32_t s_uses = 0, o_uses = 0;
+    uint32_t s_cnt = 0, o_uses = 0;
     bool ok = true;
-    for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
+    // Tiles without blocks (every key masked for the whole query block)
+    // get O = 0 and LSE = -inf directly.
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) {
       const Tile t = decode_tile(p, T);
+      if (t.n > 0) continue;
       const int64_t orow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
-      __nv_bfloat16* optr = p.o + orow * D;
-      int64_t lo = 0, hi = 0;
-      if (p.mi.kind != BSA_MASK_DENSE) {
-        const int64_t q = p.mi.q_sequence[t.i * 128 + r];
-        key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, q, lo, hi);
-      }
-      float m = -INFINITY, l = 0.f;
-      uint32_t exec = 0;
-      RowWalk w;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
+      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      p.lse[orow] = -INFINITY;
+    }
+    uint32_t total = 0;
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(decode_tile(p, T).n);
+    float m = -INFINITY, l = 0.f;
+    int64_t lo = 0, hi = 0;
+    uint32_t exec = 0;
+    Tile tt{};
+    while (ok && s_cnt < total) {
+      const uint32_t sb = s_cnt % kSBufs;
+      if (!mbar_wait_warp(&s.s_full[sb], (s_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
+      // block descriptor published by the K producer before this block's K load
+      const uint4 bi = s.binfo[s_cnt % kInfoRing];
       BlockRef br;
-      while (t.n > 0 && w.next(p, t, br)) {
-        const uint32_t sb = s_uses & 1u;
-        if (!mbar_wait_warp(&s.s_full[sb], (s_uses >> 1) & 1u, wc)) { ok = false; break; }
-        tc_fence_after();
-        float x[128];
-        {
-          uint32_t xu[128];
-          const uint32_t sa = tmem + kTmemS + sb * 128 + lane_off;
-          tmem_ld32(sa + 0, xu + 0);
-          tmem_ld32(sa + 32, xu + 32);
-          tmem_ld32(sa + 64, xu + 64);
-          tmem_ld32(sa + 96, xu + 96);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xu[c]);
+      br.col = static_cast<int32_t>(bi.x & 0xFFFFu);
+      br.label = static_cast<int32_t>((bi.x >> 16) & 3u);
+      br.slot = static_cast<int32_t>(bi.y);
+      const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
+      if (first) {
+        tt = decode_tile(p, static_cast<int32_t>(bi.z));
+        m = -INFINITY;
+        l = 0.f;
+        exec = 0;
+        if (p.mi.kind != BSA_MASK_DENSE) {
+          const int64_t q = p.mi.q_sequence[tt.i * 128 + r];
+          key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, q, lo, hi);
         }
-        if (br.label == 1) {
-          if (p.mi.kind == BSA_MASK_DENSE) {
-            const uint4* mrow = reinterpret_cast<const uint4*>(p.mi.partial + (static_cast<int64_t>(br.slot) * 128 + r) * 128);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const uint4 mw = __ldg(mrow + v);
-              const uint32_t wv[4] = {mw.x, mw.y, mw.z, mw.w};
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                if (((wv[e >> 2] >> ((e & 3) * 8)) & 0xFFu) == 0u) x[v * 16 + e] = -INFINITY;
-            }
-          } else {
-            const int64_t k0 = static_cast<int64_t>(br.col) * 128;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-              const int64_t k = k0 + c;
-              if (k < lo || k > hi) x[c] = -INFINITY;
-            }
-          }
-        }
-        float mx = x[0];
-#pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
-        const float m_blk = mx * scale_log2;
-        const float m_cand = fmaxf(m, m_blk);
-        bool switch_ref = m_cand > m + kRescaleThreshold;
-        const bool warp_switch = __any_sync(0xffffffffu, switch_ref);
-        float alpha = 1.f;
-        if (warp_switch) {
-          alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_cand);
-          m = m_cand;
-        }
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        float rs = 0.f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(x[2 * c], scale_log2, -m_use));
-          const float p1 = ex2_approx(fmaf(x[2 * c + 1], scale_log2, -m_use));
-          rs += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        l = l * alpha + rs;
-        // O holds earlier blocks' sum only after the first block; rescale it
-        // (after the previous P V has landed) when this warp moved its max.
-        if (warp_switch && exec > 0) {
-          if (!mbar_wait_warp(&s.pv_done, (s_uses - 1) & 1u, wc)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            const uint32_t oa = tmem + kTmemO + c * 32 + lane_off;
-            tmem_ld32(oa, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(oa, ov);
-          }
-        }
-        {
-          const uint32_t pa = tmem + kTmemS + sb * 128 + lane_off;
-          tmem_st32(pa + 0, pk + 0);
-          tmem_st32(pa + 32, pk + 32);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&s.p_full[sb]);
-        ++s_uses;
-        ++exec;
       }
-      if (!ok) break;
-      // ---------------------------------------------------------- epilogue
-      if (exec > 0) {
-        if (!mbar_wait_warp(&s.o_full, o_uses & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t xu[128];
+      {
+        const uint32_t sa = tmem + sb * 128 + lane_off;
+        tmem_ld32(sa + 0, xu + 0);
+        tmem_ld32(sa + 32, xu + 32);
+        tmem_ld32(sa + 64, xu + 64);
+        tmem_ld32(sa + 96, xu + 96);
+      }
+      uint32_t mbits[4] = {~0u, ~0u, ~0u, ~0u};  // visibility of the 128 columns (label 1 only)
+      if (br.label == 1) {
+        if (p.mi.kind == BSA_MASK_DENSE) {
+          const uint4* mrow = reinterpret_cast<const uint4*>(p.mi.partial + (static_cast<int64_t>(br.slot) * 128 + r) * 128);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 mw = __ldg(mrow + v);
+            const uint32_t wv[4] = {mw.x, mw.y, mw.z, mw.w};
+            uint32_t bits = 0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) bits |= (((wv[e >> 2] >> ((e & 3) * 8)) & 0xFFu) != 0u ? 1u : 0u) << e;
+            if (v & 1) mbits[v >> 1] |= bits << 16;
+            else mbits[v >> 1] = bits;
+          }
+        } else {
+          // visible columns of this row form [a, b] inside the block
+          const int64_t k0 = static_cast<int64_t>(br.col) * 128;
+          const int64_t a64 = lo - k0, b64 = hi - k0;
+          const int32_t a = a64 < 0 ? 0 : (a64 > 128 ? 128 : static_cast<int32_t>(a64));
+          const int32_t b = b64 > 127 ? 127 : (b64 < -1 ? -1 : static_cast<int32_t>(b64));
+#pragma unroll
+          for (int w32 = 0; w32 < 4; ++w32) {
+            const int32_t lo_c = a - w32 * 32, hi_c = b - w32 * 32;  // inclusive range in this word
+            uint32_t bits = 0;
+            if (hi_c >= 0 && lo_c <= 31 && hi_c >= lo_c) {
+              const int32_t l0 = lo_c < 0 ? 0 : lo_c, h0 = hi_c > 31 ? 31 : hi_c;
+              const uint32_t upto = h0 >= 31 ? 0xFFFFFFFFu : ((1u << (h0 + 1)) - 1u);
+              bits = upto & ~((1u << l0) - 1u);
+            }
+            mbits[w32] = bits;
+          }
+        }
+      }
+      tmem_wait_ld();
+      if (br.label == 1) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (!((mbits[c >> 5] >> (c & 31)) & 1u)) xu[c] = 0xFF800000u;  // -inf
+      }
+      // row max: four independent chains of three-input maxima
+      float m0 = __uint_as_float(xu[0]), m1 = __uint_as_float(xu[1]);
+      float m2 = __uint_as_float(xu[2]), m3 = __uint_as_float(xu[3]);
+#pragma unroll
+      for (int c = 4; c < 128; c += 8) {
+        m0 = fmax3(m0, __uint_as_float(xu[c + 0]), __uint_as_float(xu[c + 1]));
+        m1 = fmax3(m1, __uint_as_float(xu[c + 2]), __uint_as_float(xu[c + 3]));
+        m2 = fmax3(m2, __uint_as_float(xu[c + 4]), __uint_as_float(xu[c + 5]));
+        m3 = fmax3(m3, __uint_as_float(xu[c + 6]), __uint_as_float(xu[c + 7]));
+      }
+      const float mx = fmax3(fmaxf(m0, m1), m2, m3);
+      const float m_blk = mx * scale_log2;
+      const float m_cand = fmaxf(m, m_blk);
+      const bool switch_ref = m_cand > m + kRescaleThreshold;
+      const bool warp_switch = __any_sync(0xffffffffu, switch_ref);
+      float alpha = 1.f;
+      if (warp_switch) {
+        alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_cand);
+        m = m_cand;
+      }
+      const float m_use = (m == -INFINITY) ? 0.f : m;
+      // p = exp2(s * scale_log2 - m): packed FMA, four packed partial sums
+      const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_use, -m_use);
+      uint64_t acc[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) acc[a] = f2_pack(0.f, 0.f);
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const uint64_t e2 = f2_fma(f2_pack(__uint_as_float(xu[2 * c]), __uint_as_float(xu[2 * c + 1])), sc2, nm2);
+        float e0, e1;
+        f2_unpack(e2, e0, e1);
+        const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+        acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      const uint64_t acc01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+      float rs0, rs1;
+      f2_unpack(acc01, rs0, rs1);
+      l = l * alpha + (rs0 + rs1);
+      {
+        const uint32_t pa = tmem + sb * 128 + lane_off;
+        tmem_st32(pa + 0, pk + 0);
+        tmem_st32(pa + 32, pk + 32);
+      }
+      // O holds earlier blocks' sum only after the first block; rescale it
+      // (after the previous P V has landed) when this warp moved its max.
+      if (warp_switch && exec > 0) {
+        const uint32_t prev = s_cnt - 1;
+        if (!mbar_wait_warp(&s.pv_done[prev % kSBufs], (prev / kSBufs) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(tmem + kTmemO + c * 32 + lane_off, ov);
+          const uint32_t oa = tmem + kTmemO + c * 32 + lane_off;
+          tmem_ld32(oa, ov);
           tmem_wait_ld();
-          uint4* dst = reinterpret_cast<uint4*>(optr + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o4;
-            o4.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l);
-            o4.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l);
-            o4.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l);
-            o4.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l);
-            dst[v] = o4;
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t o2 = f2_mul(f2_pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), al2);
+            float a0, a1;
+            f2_unpack(o2, a0, a1);
+            ov[e] = __float_as_uint(a0);
+            ov[e + 1] = __float_as_uint(a1);
           }
+          tmem_st32(oa, ov);
         }
-        tc_fence_before();
-        mbar_arrive(&s.o_empty);
-        ++o_uses;
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        p.lse[orow] = l > 0.f ? (m_use + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-      } else {
-        uint4* dst = reinterpret_cast<uint4*>(optr);
-        for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
-        p.lse[orow] = -INFINITY;
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.p_full[sb]);
+      ++s_cnt;
+      ++exec;
+      if (!last) continue;
+      // ---------------------------------------------------------- epilogue
+      const int64_t orow = (static_cast<int64_t>(tt.b) * p.Hq + tt.hq) * p.Sq + static_cast<int64_t>(tt.i) * 128 + r;
+      __nv_bfloat16* optr = p.o + orow * D;
+      if (!mbar_wait_warp(&s.o_full, o_uses & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tmem + kTmemO + c * 32 + lane_off, ov);
+        tmem_wait_ld();
+        uint4* dst = reinterpret_cast<uint4*>(optr + c * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 o4;
+          o4.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l);
+          o4.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l);
+          o4.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l);
+          o4.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l);
+          dst[v] = o4;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.o_empty);
+      ++o_uses;
+      p.lse[orow] = l > 0.f ? (m_use + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     }
   }
 

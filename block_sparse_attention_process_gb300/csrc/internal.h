@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <string>
 
-#include "../../include/bsa.h"
+#include "bsa.h"
 
 // Compiled mask, owned by the library.
 struct bsa_mask_info {

@@ -3,7 +3,7 @@
 #pragma once
 #include <cstdint>
 
-#include "../../include/bsa.h"
+#include "bsa.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -61,11 +61,24 @@ struct BlockRef {
   int32_t slot;   // stack slot for dense label-1 blocks, else 0
 };
 
-__device__ __forceinline__ BlockRef read_block(const MaskInfoDev& m, int64_t row_base, int t, uint32_t* err) {
-  BlockRef r;
+// Unchecked entry as loaded (so that the load can be issued ahead of use).
+struct RawRef {
+  int32_t label, col, slot;
+};
+
+__device__ __forceinline__ RawRef load_block(const MaskInfoDev& m, int64_t row_base, int t) {
+  RawRef r;
   r.label = m.block_mask[row_base + t];
   r.col = load_idx(m.data_next, m.dn_bytes, row_base + t);
   r.slot = m.mask_next ? load_idx(m.mask_next, m.mn_bytes, row_base + t) : 0;
+  return r;
+}
+
+__device__ __forceinline__ BlockRef check_block(const MaskInfoDev& m, const RawRef& raw, uint32_t* err) {
+  BlockRef r;
+  r.label = raw.label;
+  r.col = raw.col;
+  r.slot = raw.slot;
   bool bad = r.label < 0 || r.label > 2 || r.col < 0 || r.col >= m.cols;
   if (m.mask_next && r.label == 1) bad |= r.slot < 0 || r.slot >= m.num_partial;
   if (bad) {
@@ -75,6 +88,10 @@ __device__ __forceinline__ BlockRef read_block(const MaskInfoDev& m, int64_t row
     r.slot = 0;
   }
   return r;
+}
+
+__device__ __forceinline__ BlockRef read_block(const MaskInfoDev& m, int64_t row_base, int t, uint32_t* err) {
+  return check_block(m, load_block(m, row_base, t), err);
 }
 
 constexpr int64_t kMaskInf = int64_t(1) << 40;
