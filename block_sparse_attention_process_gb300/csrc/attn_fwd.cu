@@ -19,8 +19,10 @@
 //               blocks ahead of the P V it is waiting for, and O += P V
 //               with P read from TMEM (bf16 over its score buffer)
 //   warp 2      TMA producer of V blocks (2 stages)
-//   warps 4-7   softmax, one query row per thread: mask, row max, exp2,
-//               row sum, P to TMEM, lazy O rescale in TMEM, epilogue
+//   warps 4-11  softmax in two warpgroups, one (row, half of the columns)
+//               per thread: mask, row max (halves exchanged through shared
+//               memory), exp2, row sum, P to TMEM, lazy O rescale in TMEM,
+//               epilogue
 // Each CTA walks one fixed sequence of (tile, block) pairs; every role
 // walks it the same way, so the pipelines stay in step without sharing
 // state.  Work tiles are (batch, query head, query block), longest rows
@@ -36,12 +38,11 @@
 namespace bsa {
 namespace {
 
-constexpr int kStagesK = 3;
-static_assert(kStagesK == 3, "the K stage of block n is released by the S buffer barrier of block n");
+constexpr int kStagesK = 2;
 constexpr int kStagesV = 2;
-constexpr int kSBufs = 3;         // score buffers in TMEM (== K stages: S complete frees its K stage)
+constexpr int kSBufs = 3;         // score buffers in TMEM
 constexpr int kInfoRing = 16;     // block descriptors published by the K producer
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // 4 role warps + 8 softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 384;  // O accumulator after three 128-column score buffers
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by more
@@ -53,11 +54,13 @@ struct __align__(1024) FwdSmem {
   uint8_t k[kStagesK][kTileBytes];
   uint8_t v[kStagesV][kTileBytes];
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStagesK];
+  uint64_t k_full[kStagesK], k_empty[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t o_full, o_empty, drain;
   uint4 binfo[kInfoRing];  // per block: {col | label<<16 | first<<20 | last<<21, slot, tile, 0}
+  float xmax[2][2][128];    // partial row maxima per [block parity][half][row]
+  float xsum[2][128];       // partial row sums per [half][row] at the epilogue
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -182,16 +185,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.p_full[i], 256);
       mbar_init(&s.pv_done[i], 1);
     }
-    for (int i = 0; i < kStagesK; ++i) mbar_init(&s.k_full[i], 1);
+    for (int i = 0; i < kStagesK; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+    }
     for (int i = 0; i < kStagesV; ++i) {
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_empty[i], 1);
     }
     mbar_init(&s.o_full, 1);
-    mbar_init(&s.o_empty, 128);
+    mbar_init(&s.o_empty, 256);
     mbar_init(&s.drain, 1);
     fence_mbar_init();
   }
@@ -230,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           kv_base = (static_cast<int64_t>(sq.t.b) * p.Hkv + sq.t.hq / (p.Hq / p.Hkv)) * p.Skv;
         }
         const uint32_t ks = k_loads % kStagesK;
-        if (k_loads >= kStagesK && !mbar_wait(&s.s_full[ks], ((k_loads / kStagesK) - 1) & 1u, wc)) { ok = false; break; }
+        if (k_loads >= kStagesK && !mbar_wait(&s.k_empty[ks], ((k_loads / kStagesK) - 1) & 1u, wc)) { ok = false; break; }
         s.binfo[k_loads % kInfoRing] =
             make_uint4(static_cast<uint32_t>(br.col) | (static_cast<uint32_t>(br.label) << 16) | (first ? 1u << 20 : 0u) |
                            (last ? 1u << 21 : 0u),
@@ -312,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
         mma_ss_elect(tmem + sb * 128, cur_q + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
-      mma_commit_elect(&s.s_full[sb]);  // also frees K stage ks
+      mma_commit_elect(&s.s_full[sb]);
+      mma_commit_elect(&s.k_empty[ks]);
       if (info & (1u << 21)) {          // last block of the tile: its Q buffer is free after this S
         mma_commit_elect(&s.q_empty[q_uses & 1u]);
         ++q_uses;
@@ -352,9 +359,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
     (void)mbar_wait(&s.drain, 0, dw);
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax
-    const int r = static_cast<int>(threadIdx.x) - 128;  // query row in the tile == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // ------------------------------------------------------------ softmax (two warpgroups)
+    // Warpgroup `half` takes score columns [64*half, 64*half+64) of every
+    // row; warps w and w+4 share TMEM lanes (rows) and exchange their
+    // partial row maxima through shared memory under a 64-thread barrier.
+    const int half = (warp - 4) >> 2;
+    const int quarter = (warp - 4) & 3;
+    const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
+    const uint32_t bar_id = 1u + static_cast<uint32_t>(quarter);
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half) * 64;     // first score column of this half
+    constexpr int kOCols = D / 2;                               // O columns per half
+    const uint32_t ocol0 = kTmemO + static_cast<uint32_t>(half) * kOCols;
     const float scale_log2 = p.scale_log2;
     uint32_t s_cnt = 0, o_uses = 0;
     bool ok = true;
@@ -364,13 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile t = decode_tile(p, T);
       if (t.n > 0) continue;
       const int64_t orow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
-      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
-      p.lse[orow] = -INFINITY;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + half * kOCols);
+      for (int v = 0; v < kOCols / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      if (half == 0) p.lse[orow] = -INFINITY;
     }
     uint32_t total = 0;
     for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(decode_tile(p, T).n);
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // l: this half's partial row sum
     int64_t lo = 0, hi = 0;
     uint32_t exec = 0;
     Tile tt{};
@@ -379,10 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(&s.s_full[sb], (s_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
       // block descriptor published by the K producer before this block's K load
       const uint4 bi = s.binfo[s_cnt % kInfoRing];
-      BlockRef br;
-      br.col = static_cast<int32_t>(bi.x & 0xFFFFu);
-      br.label = static_cast<int32_t>((bi.x >> 16) & 3u);
-      br.slot = static_cast<int32_t>(bi.y);
+      const int32_t col = static_cast<int32_t>(bi.x & 0xFFFFu);
+      const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
         tt = decode_tile(p, static_cast<int32_t>(bi.z));
@@ -395,20 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_after();
-      uint32_t xu[128];
+      uint32_t xu[64];
       {
-        const uint32_t sa = tmem + sb * 128 + lane_off;
+        const uint32_t sa = tmem + sb * 128 + col0 + lane_off;
         tmem_ld32(sa + 0, xu + 0);
         tmem_ld32(sa + 32, xu + 32);
-        tmem_ld32(sa + 64, xu + 64);
-        tmem_ld32(sa + 96, xu + 96);
       }
-      uint32_t mbits[4] = {~0u, ~0u, ~0u, ~0u};  // visibility of the 128 columns (label 1 only)
-      if (br.label == 1) {
+      uint32_t mbits[2] = {~0u, ~0u};  // visibility of this half's 64 columns (label 1 only)
+      if (label == 1) {
         if (p.mi.kind == BSA_MASK_DENSE) {
-          const uint4* mrow = reinterpret_cast<const uint4*>(p.mi.partial + (static_cast<int64_t>(br.slot) * 128 + r) * 128);
+          const uint4* mrow = reinterpret_cast<const uint4*>(
+              p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
+          for (int v = 0; v < 4; ++v) {
             const uint4 mw = __ldg(mrow + v);
             const uint32_t wv[4] = {mw.x, mw.y, mw.z, mw.w};
             uint32_t bits = 0;
@@ -418,13 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             else mbits[v >> 1] = bits;
           }
         } else {
-          // visible columns of this row form [a, b] inside the block
-          const int64_t k0 = static_cast<int64_t>(br.col) * 128;
+          // visible columns of this row form [a, b] inside this half
+          const int64_t k0 = static_cast<int64_t>(col) * 128 + col0;
           const int64_t a64 = lo - k0, b64 = hi - k0;
-          const int32_t a = a64 < 0 ? 0 : (a64 > 128 ? 128 : static_cast<int32_t>(a64));
-          const int32_t b = b64 > 127 ? 127 : (b64 < -1 ? -1 : static_cast<int32_t>(b64));
+          const int32_t a = a64 < 0 ? 0 : (a64 > 64 ? 64 : static_cast<int32_t>(a64));
+          const int32_t b = b64 > 63 ? 63 : (b64 < -1 ? -1 : static_cast<int32_t>(b64));
 #pragma unroll
-          for (int w32 = 0; w32 < 4; ++w32) {
+          for (int w32 = 0; w32 < 2; ++w32) {
             const int32_t lo_c = a - w32 * 32, hi_c = b - w32 * 32;  // inclusive range in this word
             uint32_t bits = 0;
             if (hi_c >= 0 && lo_c <= 31 && hi_c >= lo_c) {
@@ -437,26 +450,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tmem_wait_ld();
-      if (br.label == 1) {
+      if (label == 1) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < 64; ++c)
           if (!((mbits[c >> 5] >> (c & 31)) & 1u)) xu[c] = 0xFF800000u;  // -inf
       }
-      // row max: four independent chains of three-input maxima
+      // partial row max over this half: four chains of three-input maxima
       float m0 = __uint_as_float(xu[0]), m1 = __uint_as_float(xu[1]);
       float m2 = __uint_as_float(xu[2]), m3 = __uint_as_float(xu[3]);
 #pragma unroll
-      for (int c = 4; c < 128; c += 8) {
+      for (int c = 4; c < 64; c += 8) {
         m0 = fmax3(m0, __uint_as_float(xu[c + 0]), __uint_as_float(xu[c + 1]));
         m1 = fmax3(m1, __uint_as_float(xu[c + 2]), __uint_as_float(xu[c + 3]));
         m2 = fmax3(m2, __uint_as_float(xu[c + 4]), __uint_as_float(xu[c + 5]));
         m3 = fmax3(m3, __uint_as_float(xu[c + 6]), __uint_as_float(xu[c + 7]));
       }
-      const float mx = fmax3(fmaxf(m0, m1), m2, m3);
+      const float pm = fmax3(fmaxf(m0, m1), m2, m3);
+      // exchange with the other half of the row (double-buffered by block parity)
+      s.xmax[s_cnt & 1u][half][r] = pm;
+      named_bar_sync(bar_id, 64);
+      const float mx = fmaxf(pm, s.xmax[s_cnt & 1u][half ^ 1][r]);
       const float m_blk = mx * scale_log2;
       const float m_cand = fmaxf(m, m_blk);
       const bool switch_ref = m_cand > m + kRescaleThreshold;
-      const bool warp_switch = __any_sync(0xffffffffu, switch_ref);
+      const bool warp_switch = __any_sync(0xffffffffu, switch_ref);  // same rows, same values in both halves
       float alpha = 1.f;
       if (warp_switch) {
         alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_cand);
@@ -468,9 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t acc[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) acc[a] = f2_pack(0.f, 0.f);
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const uint64_t e2 = f2_fma(f2_pack(__uint_as_float(xu[2 * c]), __uint_as_float(xu[2 * c + 1])), sc2, nm2);
         float e0, e1;
         f2_unpack(e2, e0, e1);
@@ -482,22 +499,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rs0, rs1;
       f2_unpack(acc01, rs0, rs1);
       l = l * alpha + (rs0 + rs1);
-      {
-        const uint32_t pa = tmem + sb * 128 + lane_off;
-        tmem_st32(pa + 0, pk + 0);
-        tmem_st32(pa + 32, pk + 32);
-      }
-      // O holds earlier blocks' sum only after the first block; rescale it
-      // (after the previous P V has landed) when this warp moved its max.
+      // P (bf16 pairs) over the first 64 columns of the score buffer: this
+      // half's 64 probabilities go to words [32*half, 32*half+32); both
+      // halves finished reading their scores before the exchange barrier.
+      tmem_st32(tmem + sb * 128 + static_cast<uint32_t>(half) * 32 + lane_off, pk);
+      // O holds earlier blocks' sum only after the first block; rescale this
+      // half's O columns (after the previous P V has landed) when the max moved.
       if (warp_switch && exec > 0) {
         const uint32_t prev = s_cnt - 1;
         if (!mbar_wait_warp(&s.pv_done[prev % kSBufs], (prev / kSBufs) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
         const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kOCols / 32; ++c) {
           uint32_t ov[32];
-          const uint32_t oa = tmem + kTmemO + c * 32 + lane_off;
+          const uint32_t oa = tmem + ocol0 + c * 32 + lane_off;
           tmem_ld32(oa, ov);
           tmem_wait_ld();
 #pragma unroll
@@ -518,15 +534,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++exec;
       if (!last) continue;
       // ---------------------------------------------------------- epilogue
+      s.xsum[half][r] = l;
+      named_bar_sync(bar_id, 64);
+      const float l_row = l + s.xsum[half ^ 1][r];
       const int64_t orow = (static_cast<int64_t>(tt.b) * p.Hq + tt.hq) * p.Sq + static_cast<int64_t>(tt.i) * 128 + r;
-      __nv_bfloat16* optr = p.o + orow * D;
+      __nv_bfloat16* optr = p.o + orow * D + half * kOCols;
       if (!mbar_wait_warp(&s.o_full, o_uses & 1u, wc)) { ok = false; break; }
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kOCols / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(tmem + kTmemO + c * 32 + lane_off, ov);
+        tmem_ld32(tmem + ocol0 + c * 32 + lane_off, ov);
         tmem_wait_ld();
         uint4* dst = reinterpret_cast<uint4*>(optr + c * 32);
 #pragma unroll
@@ -542,7 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&s.o_empty);
       ++o_uses;
-      p.lse[orow] = l > 0.f ? (m_use + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+      if (half == 0) p.lse[orow] = l_row > 0.f ? (m_use + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+      // the partner's read of xsum happens before its next write (next tile's epilogue)
+      // is reached, since both pass this tile's remaining exchange barriers in order
     }
   }
 

@@ -369,6 +369,11 @@ __device__ __forceinline__ uint32_t elect_one_lane() {
   return (threadIdx.x & 31u) == 0u;
 }
 
+// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ int warp_id() { return static_cast<int>(threadIdx.x >> 5); }
 
 }  // namespace bsa
