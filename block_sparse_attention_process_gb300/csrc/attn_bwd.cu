@@ -20,13 +20,19 @@
 //       S = Q K^T, dP = dO V^T, dQ += dS K
 // dK and dQ take the softmax scale at the end.
 //
-// GB300 design: warp 0 loads by TMA, warp 1 issues tcgen05 MMAs, warps 4-7
-// (one TMEM lane / tile row per thread) rebuild P and dS and write them to
-// tensor memory as bf16, where they are the A operand of the accumulating
-// MMAs.  The inner loop runs over 64-wide halves of each block so that the
-// score buffers can be double-buffered next to the two 128-column
-// accumulators (TMEM: S x2, dP x2 of 64 columns, then dV/dK or dQ): the
-// MMAs of half n+1 overlap the elementwise work of half n.
+// GB300 design (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer; also the only reader of MaskInfo: it publishes
+//               each block's descriptor into a shared-memory ring
+//   warp 1      tcgen05 issuer, warp-converged, one elected lane issues
+//   warp 2      second TMA producer (V blocks of the dQ launch)
+//   warps 4-11  two warpgroups, one (tile row, half of the 128 columns) per
+//               thread: rebuild P and dS from the scores in TMEM and write
+//               them back to TMEM as bf16, where they are the A operand of
+//               the accumulating MMAs; each half writes inside its own
+//               64-column range (words at columns [64h, 64h+32)), so the two
+//               halves never race and the MMA reads the A operand in two
+//               32-column pieces.
+// All MMAs are 128 x 128 (full rate on sm_103a).
 #include <cmath>
 
 #include "internal.h"
@@ -37,12 +43,9 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kStages = 4;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;     // S (or S^T) halves at 0 and 64
-constexpr uint32_t kColDP = 128;  // dP (or dP^T) halves at 128 and 192
-constexpr uint32_t kColAcc = 256; // dV then dK (dK/dV launch), or dQ (dQ launch)
+constexpr int kInfoRing = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
@@ -61,21 +64,10 @@ struct BwdParams {
   uint64_t wait_ns;
 };
 
-// Walk of one MaskInfo row's non-empty positions (same for every role).
-struct Walk {
-  int32_t pos = 0, taken = 0;
-  __device__ __forceinline__ bool next(const BwdParams& p, int64_t row_base, int32_t n, BlockRef& out) {
-    while (taken < n && pos < p.mi.width) {
-      const BlockRef r = read_block(p.mi, row_base, pos++, p.err);
-      if (r.label != 0) {
-        ++taken;
-        out = r;
-        return true;
-      }
-    }
-    return false;
-  }
-};
+// TMEM column of 16-bit A-operand k-step kk (16 elements = 8 columns) when
+// the two halves of a 128-wide operand sit at columns [0, 32) and [64, 96)
+// of a 128-column buffer.
+__device__ __forceinline__ uint32_t split_a_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
 __device__ __forceinline__ void store_row(void* base, int fp32, int64_t row, int D, const uint32_t* v, int c0,
                                           float mul) {
@@ -100,42 +92,17 @@ __device__ __forceinline__ void store_row(void* base, int fp32, int64_t row, int
   }
 }
 
-__device__ __forceinline__ void store_zero_row(void* base, int fp32, int64_t row, int D) {
+__device__ __forceinline__ void store_zero_cols(void* base, int fp32, int64_t row, int D, int c0, int n) {
   if (fp32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row * D);
-    for (int e = 0; e < D / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row * D + c0);
+    for (int e = 0; e < n / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row * D);
-    for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row * D + c0);
+    for (int e = 0; e < n / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
   }
 }
 
-// Elementwise core shared by both launches: for 64 columns of one row,
-// P = exp2(S*scale_log2 - lse2) where visible (else 0), dS = P*(dP - dsum),
-// packed to bf16 pairs.  `allowed` bit c says column c is visible.
-template <bool kPerColumnStats>
-__device__ __forceinline__ void p_ds_64(const uint32_t* s, const uint32_t* dp, uint64_t allowed, float scale_log2,
-                                        float lse2_row, float dsum_row, const float* lse2_col,
-                                        const float* dsum_col, uint32_t* p_pk, uint32_t* ds_pk) {
-#pragma unroll
-  for (int c = 0; c < 64; c += 2) {
-    float pv[2], dv[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int cc = c + e;
-      const float l2 = kPerColumnStats ? lse2_col[cc] : lse2_row;
-      const float ds_ = kPerColumnStats ? dsum_col[cc] : dsum_row;
-      const float pe = ex2_approx(fmaf(__uint_as_float(s[cc]), scale_log2, -l2));
-      const float pm = ((allowed >> cc) & 1ull) ? pe : 0.f;
-      pv[e] = pm;
-      dv[e] = pm * (__uint_as_float(dp[cc]) - ds_);
-    }
-    if (p_pk) p_pk[c >> 1] = pack_bf16x2(pv[0], pv[1]);
-    ds_pk[c >> 1] = pack_bf16x2(dv[0], dv[1]);
-  }
-}
-
-// Visibility bits of 64 consecutive columns for one row of a label-1 block.
+// Visibility bits of 64 consecutive columns of one row of a stacked block.
 __device__ __forceinline__ uint64_t dense_bits_64(const uint8_t* row64) {
   uint64_t bits = 0;
   const uint4* src = reinterpret_cast<const uint4*>(row64);
@@ -160,23 +127,434 @@ __device__ __forceinline__ uint64_t interval_bits_64(int64_t c0, int64_t lo, int
   return run << a;
 }
 
+__device__ __forceinline__ uint32_t pack_info(int32_t col, int32_t label, bool first, bool last) {
+  return static_cast<uint32_t>(col) | (static_cast<uint32_t>(label) << 16) | (first ? 1u << 20 : 0u) |
+         (last ? 1u << 21 : 0u);
+}
+
 // ===========================================================================
-// dK / dV
+// dQ launch
 // ===========================================================================
+constexpr int kDqStagesK = 3;   // S is issued two blocks ahead of the dQ MMA that frees its K
+constexpr int kDqStagesV = 2;
+constexpr uint32_t kDqColS = 0;     // two S buffers at 0 and 128
+constexpr uint32_t kDqColDP = 256;  // dP, then dS (bf16) over it
+constexpr uint32_t kDqColQ = 384;   // dQ accumulator
+
+template <int D>
+struct __align__(1024) DqSmem {
+  static constexpr int kTile = 128 * D * 2;
+  uint8_t q[kTile];
+  uint8_t dout[kTile];
+  uint8_t k[kDqStagesK][kTile];
+  uint8_t v[kDqStagesV][kTile];
+  uint64_t qo_full, qo_empty;
+  uint64_t k_full[kDqStagesK], k_empty[kDqStagesK];
+  uint64_t v_full[kDqStagesV], v_empty[kDqStagesV];
+  uint64_t s_full[2], dp_full, ds_full;
+  uint64_t acc_full, acc_empty, drain;
+  uint4 binfo[kInfoRing];  // {col | label<<16 | first<<20 | last<<21, slot, tile, 0}
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+struct DqTile {
+  int32_t b, hq, i, hm, n;
+  int64_t row_base;
+};
+
+__device__ __forceinline__ DqTile dq_decode(const BwdParams& p, int32_t T) {
+  DqTile t;
+  if (p.mi.heads == 1) {
+    const int32_t bh = T % (p.B * p.Hq);
+    t.i = p.mi.row_order[T / (p.B * p.Hq)];
+    t.b = bh / p.Hq;
+    t.hq = bh % p.Hq;
+    t.hm = 0;
+  } else {
+    t.b = T % p.B;
+    const int32_t row = p.mi.row_order[T / p.B];
+    t.hm = row / p.mi.rows;
+    t.i = row % p.mi.rows;
+    t.hq = t.hm;
+  }
+  t.n = p.mi.row_len[t.hm * p.mi.rows + t.i];
+  t.row_base = (static_cast<int64_t>(t.hm) * p.mi.rows + t.i) * p.mi.width;
+  return t;
+}
+
+// Cursor over the CTA's (tile, block) sequence of the dQ launch (tiles
+// without blocks skipped; each tile yields exactly row_len blocks).
+struct DqSeq {
+  int32_t T, j, pos;
+  DqTile t;
+  RawRef ahead;
+  bool valid;
+  __device__ __forceinline__ void start_tile(const BwdParams& p) {
+    while (true) {
+      T += gridDim.x;
+      if (T >= p.n_tiles) {
+        valid = false;
+        return;
+      }
+      t = dq_decode(p, T);
+      if (t.n > 0) break;
+    }
+    j = 0;
+    pos = 0;
+    if (p.mi.width > 0) ahead = load_block(p.mi, t.row_base, 0);
+    valid = true;
+  }
+  __device__ __forceinline__ void init(const BwdParams& p) {
+    T = static_cast<int32_t>(blockIdx.x) - static_cast<int32_t>(gridDim.x);
+    start_tile(p);
+  }
+  __device__ __forceinline__ bool next(const BwdParams& p, BlockRef& br, bool& first, bool& last) {
+    if (!valid) return false;
+    bool found = false;
+    while (pos < p.mi.width) {
+      const RawRef cur = ahead;
+      ++pos;
+      if (pos < p.mi.width) ahead = load_block(p.mi, t.row_base, pos);
+      br = check_block(p.mi, cur, p.err);
+      if (br.label != 0) {
+        found = true;
+        break;
+      }
+    }
+    if (!found) {
+      if (p.err) atomicOr(p.err, DEV_ERR_BOUNDS);
+      br.label = 2;
+      br.col = 0;
+      br.slot = 0;
+    }
+    first = j == 0;
+    ++j;
+    last = j == t.n;
+    return true;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  using Smem = DqSmem<D>;
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr uint32_t kTile = Smem::kTile;
+  constexpr int kChunks = D / 64;
+  const int warp = warp_id();
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    mbar_init(&s.qo_full, 1);
+    mbar_init(&s.qo_empty, 1);
+    for (int i = 0; i < kDqStagesK; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+    }
+    for (int i = 0; i < kDqStagesV; ++i) {
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_empty[i], 1);
+    }
+    mbar_init(&s.s_full[0], 1);
+    mbar_init(&s.s_full[1], 1);
+    mbar_init(&s.dp_full, 1);
+    mbar_init(&s.ds_full, 256);
+    mbar_init(&s.acc_full, 1);
+    mbar_init(&s.acc_empty, 256);
+    mbar_init(&s.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------ Q/dO (per tile) and K (per block); block ring
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_do);
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      uint32_t qo_loads = 0, k_loads = 0;
+      bool ok = true;
+      DqSeq sq;
+      sq.init(p);
+      BlockRef br;
+      bool first, last;
+      int64_t kv_base = 0;
+      while (ok && sq.next(p, br, first, last)) {
+        if (first) {
+          if (qo_loads >= 1 && !mbar_wait(&s.qo_empty, (qo_loads - 1) & 1u, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.qo_full, 2 * kTile);
+          const int32_t qrow = static_cast<int32_t>((static_cast<int64_t>(sq.t.b) * p.Hq + sq.t.hq) * p.Sq + sq.t.i * 128);
+          for (int c = 0; c < kChunks; ++c) {
+            tma_load_2d(s.q + c * 16384, &tm_q, &s.qo_full, c * 64, qrow, pol_q);
+            tma_load_2d(s.dout + c * 16384, &tm_do, &s.qo_full, c * 64, qrow, pol_q);
+          }
+          ++qo_loads;
+          kv_base = (static_cast<int64_t>(sq.t.b) * p.Hkv + sq.t.hq / (p.Hq / p.Hkv)) * p.Skv;
+        }
+        const uint32_t ks = k_loads % kDqStagesK;
+        if (k_loads >= kDqStagesK && !mbar_wait(&s.k_empty[ks], ((k_loads / kDqStagesK) - 1) & 1u, wc)) { ok = false; break; }
+        s.binfo[k_loads % kInfoRing] =
+            make_uint4(pack_info(br.col, br.label, first, last), static_cast<uint32_t>(br.slot),
+                       static_cast<uint32_t>(sq.T), 0u);
+        mbar_arrive_expect_tx(&s.k_full[ks], kTile);
+        const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
+        for (int c = 0; c < kChunks; ++c) tma_load_2d(s.k[ks] + c * 16384, &tm_k, &s.k_full[ks], c * 64, krow, pol_kv);
+        ++k_loads;
+        if (last) sq.start_tile(p);
+      }
+      if (!ok) {
+        uint32_t dummy_abort = 0;
+        WaitCtl dw{nullptr, &dummy_abort, p.wait_ns};
+        if (qo_loads) (void)mbar_wait(&s.qo_full, (qo_loads - 1) & 1u, dw);
+        for (uint32_t i = (k_loads > kDqStagesK ? k_loads - kDqStagesK : 0); i < k_loads; ++i)
+          (void)mbar_wait(&s.k_full[i % kDqStagesK], (i / kDqStagesK) & 1u, dw);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------ V (per block)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_kv = policy_evict_last();
+      uint32_t v_loads = 0;
+      bool ok = true;
+      DqSeq sq;
+      sq.init(p);
+      BlockRef br;
+      bool first, last;
+      int64_t kv_base = 0;
+      while (ok && sq.next(p, br, first, last)) {
+        if (first) kv_base = (static_cast<int64_t>(sq.t.b) * p.Hkv + sq.t.hq / (p.Hq / p.Hkv)) * p.Skv;
+        const uint32_t vs = v_loads % kDqStagesV;
+        if (v_loads >= kDqStagesV && !mbar_wait(&s.v_empty[vs], ((v_loads / kDqStagesV) - 1) & 1u, wc)) { ok = false; break; }
+        mbar_arrive_expect_tx(&s.v_full[vs], kTile);
+        const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
+        for (int c = 0; c < kChunks; ++c) tma_load_2d(s.v[vs] + c * 16384, &tm_v, &s.v_full[vs], c * 64, krow, pol_kv);
+        ++v_loads;
+        if (last) sq.start_tile(p);
+      }
+      if (!ok) {
+        uint32_t dummy_abort = 0;
+        WaitCtl dw{nullptr, &dummy_abort, p.wait_ns};
+        for (uint32_t i = (v_loads > kDqStagesV ? v_loads - kDqStagesV : 0); i < v_loads; ++i)
+          (void)mbar_wait(&s.v_full[i % kDqStagesV], (i / kDqStagesV) & 1u, dw);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (whole warp)
+    // order: S0 dP0 S1 | dQ0 dP1 S2 | dQ1 dP2 S3 | ...
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
+    constexpr uint64_t kTileDesc = kTile >> 4;
+    const uint64_t qdesc = sdesc_sw128(smem_u32(s.q), 16, 1024);
+    const uint64_t dodesc = sdesc_sw128(smem_u32(s.dout), 16, 1024);
+    const uint64_t kdesc0 = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
+    const uint64_t kmn0 = sdesc_sw128(smem_u32(s.k[0]), 16384, 1024);
+    const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v[0]), 16, 1024);
+    uint32_t total = 0;
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dq_decode(p, T).n);
+    uint32_t s_cnt = 0, dp_cnt = 0, q_uses = 0, acc_uses = 0;
+    bool ok = true;
+    auto k_ready = [&](uint32_t n) -> bool {
+      return mbar_wait_warp(&s.k_full[n % kDqStagesK], (n / kDqStagesK) & 1u, wc);
+    };
+    auto issue_s = [&]() -> bool {  // S_n = Q K_n^T
+      const uint32_t n = s_cnt;
+      if (!k_ready(n)) return false;
+      const uint32_t info = s.binfo[n % kInfoRing].x;
+      if ((info >> 20) & 1u) {  // first block of a tile: wait for its Q/dO
+        if (!mbar_wait_warp(&s.qo_full, q_uses & 1u, wc)) return false;
+        ++q_uses;
+      }
+      tc_fence_after();
+      const uint64_t kd = kdesc0 + (n % kDqStagesK) * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+        mma_ss_elect(tmem + kDqColS + (n & 1u) * 128, qdesc + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(&s.s_full[n & 1u]);
+      ++s_cnt;
+      return true;
+    };
+    auto issue_dp = [&]() -> bool {  // dP_n = dO V_n^T
+      const uint32_t n = dp_cnt;
+      const uint32_t vs = n % kDqStagesV;
+      if (!mbar_wait_warp(&s.v_full[vs], (n / kDqStagesV) & 1u, wc)) return false;
+      tc_fence_after();
+      const uint64_t vd = vdesc0 + vs * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+        mma_ss_elect(tmem + kDqColDP, dodesc + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(&s.dp_full);
+      mma_commit_elect(&s.v_empty[vs]);
+      const uint32_t info = s.binfo[n % kInfoRing].x;
+      if ((info >> 21) & 1u) mma_commit_elect(&s.qo_empty);  // last S and dP of the tile are issued
+      ++dp_cnt;
+      return true;
+    };
+    if (total > 0) {
+      ok = issue_s() && issue_dp();
+      if (ok && total > 1) ok = issue_s();
+    }
+    for (uint32_t n = 0; ok && n < total; ++n) {
+      const uint32_t info = s.binfo[n % kInfoRing].x;
+      const bool first = (info >> 20) & 1u, last = (info >> 21) & 1u;
+      if (!mbar_wait_warp(&s.ds_full, n & 1u, wc)) { ok = false; break; }
+      if (first && acc_uses > 0 && !mbar_wait_warp(&s.acc_empty, (acc_uses - 1) & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      // dQ += dS K_n  (dS in the dP buffer, K_n as an MN-major B operand)
+      const uint64_t kmn = kmn0 + (n % kDqStagesK) * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_elect(tmem + kDqColQ, tmem + kDqColDP + split_a_col(kk), kmn + static_cast<uint64_t>(kk * 2048 >> 4),
+                     idesc_acc, (first && kk == 0) ? 0u : 1u);
+      mma_commit_elect(&s.k_empty[n % kDqStagesK]);
+      if (last) {
+        mma_commit_elect(&s.acc_full);
+        ++acc_uses;
+      }
+      if (dp_cnt < total && !issue_dp()) { ok = false; break; }
+      if (s_cnt < total && !issue_s()) { ok = false; break; }
+    }
+    mma_commit_elect(&s.drain);
+    uint32_t dummy_abort = 0;
+    WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
+    (void)mbar_wait(&s.drain, 0, dw);
+  } else if (warp >= 4) {
+    // ------------------------------------------------ P and dS (two warpgroups)
+    const int half = (warp - 4) >> 2;
+    const int quarter = (warp - 4) & 3;
+    const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half) * 64;
+    constexpr int kHalfD = D / 2;
+    const float scale_log2 = p.scale_log2;
+    uint32_t n = 0, acc_uses = 0;
+    bool ok = true;
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) {
+      const DqTile t = dq_decode(p, T);
+      if (t.n > 0) continue;
+      const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
+      store_zero_cols(p.dq, p.grad_fp32, qrow, D, half * kHalfD, kHalfD);
+    }
+    uint32_t total = 0;
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dq_decode(p, T).n);
+    float lse2 = 0.f, dsum_r = 0.f;
+    int64_t lo = 0, hi = 0, qrow = 0;
+    for (; ok && n < total; ++n) {
+      const uint32_t sb = n & 1u;
+      if (!mbar_wait_warp(&s.s_full[sb], (n >> 1) & 1u, wc)) { ok = false; break; }
+      const uint4 bi = s.binfo[n % kInfoRing];
+      const int32_t col = static_cast<int32_t>(bi.x & 0xFFFFu);
+      const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
+      const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
+      if (first) {
+        const DqTile t = dq_decode(p, static_cast<int32_t>(bi.z));
+        qrow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
+        lse2 = p.lse[qrow] * kLog2e;
+        dsum_r = p.dsum[qrow];
+        if (p.mi.kind != BSA_MASK_DENSE) {
+          const int64_t qi = p.mi.q_sequence[t.i * 128 + r];
+          key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, qi, lo, hi);
+        }
+      }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32(tmem + kDqColS + sb * 128 + col0 + lane_off, sv);
+      tmem_ld32(tmem + kDqColS + sb * 128 + col0 + 32 + lane_off, sv + 32);
+      uint64_t allowed = ~0ull;
+      if (label == 1) {
+        if (p.mi.kind == BSA_MASK_DENSE)
+          allowed = dense_bits_64(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
+        else
+          allowed = interval_bits_64(static_cast<int64_t>(col) * 128 + col0, lo, hi);
+      }
+      tmem_wait_ld();
+      float pv[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float e = ex2_approx(fmaf(__uint_as_float(sv[c]), scale_log2, -lse2));
+        pv[c] = ((allowed >> c) & 1ull) ? e : 0.f;
+      }
+      if (!mbar_wait_warp(&s.dp_full, n & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dpv[64];
+      tmem_ld32(tmem + kDqColDP + col0 + lane_off, dpv);
+      tmem_ld32(tmem + kDqColDP + col0 + 32 + lane_off, dpv + 32);
+      tmem_wait_ld();
+      uint32_t dspk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        dspk[c] = pack_bf16x2(pv[2 * c] * (__uint_as_float(dpv[2 * c]) - dsum_r),
+                              pv[2 * c + 1] * (__uint_as_float(dpv[2 * c + 1]) - dsum_r));
+      tmem_st32(tmem + kDqColDP + col0 + lane_off, dspk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.ds_full);
+      if (!last) continue;
+      if (!mbar_wait_warp(&s.acc_full, acc_uses & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kHalfD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + kDqColQ + half * kHalfD + c * 32 + lane_off, v);
+        tmem_wait_ld();
+        store_row(p.dq, p.grad_fp32, qrow, D, v, half * kHalfD + c * 32, p.scale);
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty);
+      ++acc_uses;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ===========================================================================
+// dK / dV launch
+// ===========================================================================
+constexpr int kDkvStages = 2;        // (Q, dO, LSE, Dsum) of one query block
+constexpr uint32_t kDkvColST = 0;    // S^T, then P^T (bf16) over it
+constexpr uint32_t kDkvColDP = 128;  // dP^T, then dS^T (bf16) over it
+constexpr uint32_t kDkvColDV = 256;
+constexpr uint32_t kDkvColDK = 384;
+
 template <int D>
 struct __align__(1024) DkvSmem {
   static constexpr int kTile = 128 * D * 2;
-  static constexpr int kHalf = 64 * D * 2;
   uint8_t k[kTile];
   uint8_t v[kTile];
-  uint8_t q[kStages][kHalf];
-  uint8_t dout[kStages][kHalf];
-  float lse[kStages][64];
-  float dsum[kStages][64];
+  uint8_t q[kDkvStages][kTile];
+  uint8_t dout[kDkvStages][kTile];
+  float lse[kDkvStages][128];
+  float dsum[kDkvStages][128];
   uint64_t kv_full, kv_empty;
-  uint64_t in_full[kStages], in_empty[kStages];
-  uint64_t s_full[2], p_full[2];
+  uint64_t in_full[kDkvStages], in_empty[kDkvStages];
+  uint64_t st_full, dpt_full, p_full, ds_full;
   uint64_t acc_full, acc_empty, drain;
+  uint4 binfo[kInfoRing];  // {col | label<<16 | first<<20 | last<<21, slot, tile, q head}
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -210,34 +588,55 @@ __device__ __forceinline__ DkvTile dkv_decode(const BwdParams& p, int32_t T) {
   return t;
 }
 
-// Iterates the items (q head of the group, non-empty block, half) of a
-// dK/dV tile in a fixed order; every role walks them identically.
+// Items of one dK/dV tile, in order: q heads of the group, then the
+// non-empty query blocks of that head's MaskInfo row (each yields exactly
+// row_len blocks; a malformed row is padded with flagged dummy blocks).
 struct DkvItems {
-  int32_t gh = -1, n = 0;
-  int half = 2;
-  int64_t row_base = 0;
-  Walk w;
-  BlockRef cur;
-  __device__ __forceinline__ bool next(const BwdParams& p, const DkvTile& t, int32_t& hq, BlockRef& br, int& h) {
+  int32_t gh, n, j, pos;
+  int64_t row_base;
+  RawRef ahead;
+  __device__ __forceinline__ void start_head(const BwdParams& p, const DkvTile& t) {
     const int32_t G = p.Hq / p.Hkv;
-    if (half >= 2) {
-      while (true) {
-        if (gh >= 0 && gh < G && w.next(p, row_base, n, cur)) {
-          half = 0;
-          break;
-        }
-        if (gh >= G) return false;
-        ++gh;
-        if (gh >= G) return false;
-        const int32_t hm = dkv_mask_head(p, t.g * G + gh);
-        row_base = (static_cast<int64_t>(hm) * p.mi.rows + t.j) * p.mi.width;
-        n = p.mi.row_len[hm * p.mi.rows + t.j];
-        w = Walk();
+    while (gh < G) {
+      const int32_t hm = dkv_mask_head(p, t.g * G + gh);
+      row_base = (static_cast<int64_t>(hm) * p.mi.rows + t.j) * p.mi.width;
+      n = p.mi.row_len[hm * p.mi.rows + t.j];
+      if (n > 0) break;
+      ++gh;
+    }
+    j = 0;
+    pos = 0;
+    if (gh < G && p.mi.width > 0) ahead = load_block(p.mi, row_base, 0);
+  }
+  __device__ __forceinline__ void init(const BwdParams& p, const DkvTile& t) {
+    gh = 0;
+    start_head(p, t);
+  }
+  __device__ __forceinline__ bool next(const BwdParams& p, const DkvTile& t, int32_t& hq, BlockRef& br) {
+    const int32_t G = p.Hq / p.Hkv;
+    if (gh >= G) return false;
+    bool found = false;
+    while (pos < p.mi.width) {
+      const RawRef cur = ahead;
+      ++pos;
+      if (pos < p.mi.width) ahead = load_block(p.mi, row_base, pos);
+      br = check_block(p.mi, cur, p.err);
+      if (br.label != 0) {
+        found = true;
+        break;
       }
     }
+    if (!found) {
+      if (p.err) atomicOr(p.err, DEV_ERR_BOUNDS);
+      br.label = 2;
+      br.col = 0;
+      br.slot = 0;
+    }
     hq = t.g * G + gh;
-    br = cur;
-    h = half++;
+    if (++j == n) {
+      ++gh;
+      start_head(p, t);
+    }
     return true;
   }
 };
@@ -250,6 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   using Smem = DkvSmem<D>;
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr uint32_t kTile = Smem::kTile;
   constexpr int kChunks = D / 64;
   const int warp = warp_id();
   const int lane = threadIdx.x & 31;
@@ -258,16 +658,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort_flag = 0;
     mbar_init(&s.kv_full, 1);
     mbar_init(&s.kv_empty, 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kDkvStages; ++i) {
       mbar_init(&s.in_full[i], 1);
       mbar_init(&s.in_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 128);
-    }
+    mbar_init(&s.st_full, 1);
+    mbar_init(&s.dpt_full, 1);
+    mbar_init(&s.p_full, 256);
+    mbar_init(&s.ds_full, 256);
     mbar_init(&s.acc_full, 1);
-    mbar_init(&s.acc_empty, 128);
+    mbar_init(&s.acc_empty, 256);
     mbar_init(&s.drain, 1);
     fence_mbar_init();
   }
@@ -280,9 +680,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
-  const uint32_t colDV = kColAcc, colDK = kColAcc + D;
 
   if (warp == 0) {
+    // ------------------------------------------------ K/V (per tile), Q/dO/LSE/Dsum (per item); item ring
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -296,29 +696,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const DkvTile t = dkv_decode(p, T);
         if (t.total == 0) continue;
         if (kv_loads >= 1 && !mbar_wait(&s.kv_empty, (kv_loads - 1) & 1u, wc)) { ok = false; break; }
-        mbar_arrive_expect_tx(&s.kv_full, 2 * Smem::kTile);
+        mbar_arrive_expect_tx(&s.kv_full, 2 * kTile);
         const int32_t krow = static_cast<int32_t>((static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + t.j * 128);
-        for (int c = 0; c < kChunks; ++c)
-          for (int rb = 0; rb < 2; ++rb) {
-            tma_load_2d(s.k + c * 16384 + rb * 8192, &tm_k, &s.kv_full, c * 64, krow + rb * 64, pol_kv);
-            tma_load_2d(s.v + c * 16384 + rb * 8192, &tm_v, &s.kv_full, c * 64, krow + rb * 64, pol_kv);
-          }
+        for (int c = 0; c < kChunks; ++c) {
+          tma_load_2d(s.k + c * 16384, &tm_k, &s.kv_full, c * 64, krow, pol_kv);
+          tma_load_2d(s.v + c * 16384, &tm_v, &s.kv_full, c * 64, krow, pol_kv);
+        }
         ++kv_loads;
         DkvItems it;
+        it.init(p, t);
         int32_t hq;
         BlockRef br;
-        int half;
-        while (it.next(p, t, hq, br, half)) {
-          const uint32_t st = in_loads % kStages;
-          if (in_loads >= kStages && !mbar_wait(&s.in_empty[st], ((in_loads / kStages) - 1) & 1u, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.in_full[st], 2 * Smem::kHalf + 512);
-          const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + hq) * p.Sq + br.col * 128 + half * 64;
+        for (int32_t x = 0; x < t.total && ok; ++x) {
+          it.next(p, t, hq, br);
+          const uint32_t st = in_loads % kDkvStages;
+          if (in_loads >= kDkvStages && !mbar_wait(&s.in_empty[st], ((in_loads / kDkvStages) - 1) & 1u, wc)) { ok = false; break; }
+          s.binfo[in_loads % kInfoRing] = make_uint4(pack_info(br.col, br.label, x == 0, x == t.total - 1),
+                                                     static_cast<uint32_t>(br.slot), static_cast<uint32_t>(T),
+                                                     static_cast<uint32_t>(hq));
+          mbar_arrive_expect_tx(&s.in_full[st], 2 * kTile + 1024);
+          const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + hq) * p.Sq + br.col * 128;
           for (int c = 0; c < kChunks; ++c) {
-            tma_load_2d(s.q[st] + c * 8192, &tm_q, &s.in_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
-            tma_load_2d(s.dout[st] + c * 8192, &tm_do, &s.in_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
+            tma_load_2d(s.q[st] + c * 16384, &tm_q, &s.in_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
+            tma_load_2d(s.dout[st] + c * 16384, &tm_do, &s.in_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
           }
-          bulk_load(s.lse[st], p.lse + qrow, 256, &s.in_full[st]);
-          bulk_load(s.dsum[st], p.dsum + qrow, 256, &s.in_full[st]);
+          bulk_load(s.lse[st], p.lse + qrow, 512, &s.in_full[st]);
+          bulk_load(s.dsum[st], p.dsum + qrow, 512, &s.in_full[st]);
           ++in_loads;
         }
       }
@@ -326,452 +729,185 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t dummy_abort = 0;
         WaitCtl dw{nullptr, &dummy_abort, p.wait_ns};
         if (kv_loads) (void)mbar_wait(&s.kv_full, (kv_loads - 1) & 1u, dw);
-        for (uint32_t i = (in_loads > kStages ? in_loads - kStages : 0); i < in_loads; ++i)
-          (void)mbar_wait(&s.in_full[i % kStages], (i / kStages) & 1u, dw);
+        for (uint32_t i = (in_loads > kDkvStages ? in_loads - kDkvStages : 0); i < in_loads; ++i)
+          (void)mbar_wait(&s.in_full[i % kDkvStages], (i / kDkvStages) & 1u, dw);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
-      uint32_t kv_uses = 0, in_uses = 0, items = 0, acc_uses = 0;
-      uint32_t prev_stage = 0;
-      bool ok = true;
-      auto issue_acc = [&](uint32_t x, uint32_t stage, bool first) -> bool {
-        const uint32_t b2 = x & 1u;
-        if (!mbar_wait(&s.p_full[b2], (x >> 1) & 1u, wc)) return false;
-        if (first && acc_uses > 0 && !mbar_wait(&s.acc_empty, (acc_uses - 1) & 1u, wc)) return false;
-        tc_fence_after();
-        const uint32_t dob = smem_u32(s.dout[stage]), qb = smem_u32(s.q[stage]);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + colDV, tmem + kColS + b2 * 64 + kk * 8, sdesc_sw128(dob + kk * 2048, 8192, 1024), idesc_acc,
-                 (first && kk == 0) ? 0u : 1u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + colDK, tmem + kColDP + b2 * 64 + kk * 8, sdesc_sw128(qb + kk * 2048, 8192, 1024), idesc_acc,
-                 (first && kk == 0) ? 0u : 1u);
-        mma_commit(&s.in_empty[stage]);
-        return true;
-      };
-      for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
-        const DkvTile t = dkv_decode(p, T);
-        if (t.total == 0) continue;
-        if (!mbar_wait(&s.kv_full, kv_uses & 1u, wc)) { ok = false; break; }
-        const uint32_t kb = smem_u32(s.k), vb = smem_u32(s.v);
-        uint32_t local = 0;
-        DkvItems it;
-        int32_t hq;
-        BlockRef br;
-        int half;
-        while (it.next(p, t, hq, br, half)) {
-          const uint32_t st = in_uses % kStages;
-          if (!mbar_wait(&s.in_full[st], (in_uses / kStages) & 1u, wc)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t b2 = items & 1u;
-          const uint32_t qb = smem_u32(s.q[st]), dob = smem_u32(s.dout[st]);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = (kk >> 2) * 8192 + (kk & 3) * 32;
-            mma_ss(tmem + kColS + b2 * 64, sdesc_sw128(kb + ao, 16, 1024), sdesc_sw128(qb + bo, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = (kk >> 2) * 8192 + (kk & 3) * 32;
-            mma_ss(tmem + kColDP + b2 * 64, sdesc_sw128(vb + ao, 16, 1024), sdesc_sw128(dob + bo, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&s.s_full[b2]);
-          if (local > 0 && !issue_acc(items - 1, prev_stage, local == 1)) { ok = false; break; }
-          prev_stage = st;
-          ++in_uses;
-          ++items;
-          ++local;
-        }
-        if (!ok) break;
-        mma_commit(&s.kv_empty);
+    // ------------------------------------------------ MMA issuer (whole warp)
+    // per item n: S^T dP^T | (P ready) dV | (dS ready) dK
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
+    constexpr uint64_t kTileDesc = kTile >> 4;
+    const uint64_t kdesc = sdesc_sw128(smem_u32(s.k), 16, 1024);
+    const uint64_t vdesc = sdesc_sw128(smem_u32(s.v), 16, 1024);
+    const uint64_t qdesc0 = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
+    const uint64_t qmn0 = sdesc_sw128(smem_u32(s.q[0]), 16384, 1024);
+    const uint64_t dodesc0 = sdesc_sw128(smem_u32(s.dout[0]), 16, 1024);
+    const uint64_t domn0 = sdesc_sw128(smem_u32(s.dout[0]), 16384, 1024);
+    uint32_t total = 0;
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dkv_decode(p, T).total);
+    uint32_t kv_uses = 0, acc_uses = 0;
+    bool ok = true;
+    for (uint32_t n = 0; ok && n < total; ++n) {
+      const uint32_t st = n % kDkvStages;
+      if (!mbar_wait_warp(&s.in_full[st], (n / kDkvStages) & 1u, wc)) { ok = false; break; }
+      const uint32_t info = s.binfo[n % kInfoRing].x;
+      const bool first = (info >> 20) & 1u, last = (info >> 21) & 1u;
+      if (first) {
+        if (!mbar_wait_warp(&s.kv_full, kv_uses & 1u, wc)) { ok = false; break; }
         ++kv_uses;
-        if (local > 0) {
-          if (!issue_acc(items - 1, prev_stage, local == 1)) { ok = false; break; }
-          mma_commit(&s.acc_full);
-          ++acc_uses;
-        }
       }
-      mma_commit(&s.drain);
-      uint32_t dummy_abort = 0;
-      WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
-      (void)mbar_wait(&s.drain, 0, dw);
+      tc_fence_after();
+      const uint64_t qd = qdesc0 + st * kTileDesc, dod = dodesc0 + st * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+        mma_ss_elect(tmem + kDkvColST, kdesc + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(&s.st_full);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+        mma_ss_elect(tmem + kDkvColDP, vdesc + off, dod + off, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(&s.dpt_full);
+      if (last) mma_commit_elect(&s.kv_empty);  // K and V are read by the S^T / dP^T MMAs only
+      // dV += P^T dO
+      if (!mbar_wait_warp(&s.p_full, n & 1u, wc)) { ok = false; break; }
+      if (first && acc_uses > 0 && !mbar_wait_warp(&s.acc_empty, (acc_uses - 1) & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t domn = domn0 + st * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_elect(tmem + kDkvColDV, tmem + kDkvColST + split_a_col(kk), domn + static_cast<uint64_t>(kk * 2048 >> 4),
+                     idesc_acc, (first && kk == 0) ? 0u : 1u);
+      // dK += dS^T Q
+      if (!mbar_wait_warp(&s.ds_full, n & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t qmn = qmn0 + st * kTileDesc;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_elect(tmem + kDkvColDK, tmem + kDkvColDP + split_a_col(kk), qmn + static_cast<uint64_t>(kk * 2048 >> 4),
+                     idesc_acc, (first && kk == 0) ? 0u : 1u);
+      mma_commit_elect(&s.in_empty[st]);
+      if (last) {
+        mma_commit_elect(&s.acc_full);
+        ++acc_uses;
+      }
     }
+    mma_commit_elect(&s.drain);
+    uint32_t dummy_abort = 0;
+    WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
+    (void)mbar_wait(&s.drain, 0, dw);
   } else if (warp >= 4) {
-    const int r = static_cast<int>(threadIdx.x) - 128;  // key row in the tile == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t in_uses = 0, items = 0, acc_uses = 0;
+    // ------------------------------------------------ P^T and dS^T (two warpgroups)
+    const int half = (warp - 4) >> 2;
+    const int quarter = (warp - 4) & 3;
+    const int r = quarter * 32 + lane;  // key row in the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half) * 64;  // query columns of this half
+    constexpr int kHalfD = D / 2;
+    const float scale_log2 = p.scale_log2;
     bool ok = true;
-    for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) {
       const DkvTile t = dkv_decode(p, T);
+      if (t.total > 0) continue;
       const int64_t krow = (static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + static_cast<int64_t>(t.j) * 128 + r;
-      if (t.total == 0) {
-        store_zero_row(p.dk, p.grad_fp32, krow, D);
-        store_zero_row(p.dv, p.grad_fp32, krow, D);
-        continue;
+      store_zero_cols(p.dk, p.grad_fp32, krow, D, half * kHalfD, kHalfD);
+      store_zero_cols(p.dv, p.grad_fp32, krow, D, half * kHalfD, kHalfD);
+    }
+    uint32_t total = 0;
+    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dkv_decode(p, T).total);
+    uint32_t acc_uses = 0;
+    int64_t lo = 0, hi = 0, krow = 0;
+    for (uint32_t n = 0; ok && n < total; ++n) {
+      const uint32_t st = n % kDkvStages;
+      if (!mbar_wait_warp(&s.in_full[st], (n / kDkvStages) & 1u, wc)) { ok = false; break; }
+      const uint4 bi = s.binfo[n % kInfoRing];
+      const int32_t col = static_cast<int32_t>(bi.x & 0xFFFFu);
+      const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
+      const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
+      if (first) {
+        const DkvTile t = dkv_decode(p, static_cast<int32_t>(bi.z));
+        krow = (static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + static_cast<int64_t>(t.j) * 128 + r;
+        if (p.mi.kind != BSA_MASK_DENSE)
+          query_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(t.j) * 128 + r, lo, hi);
       }
-      int64_t lo = 0, hi = 0;
-      if (p.mi.kind != BSA_MASK_DENSE)
-        query_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(t.j) * 128 + r, lo, hi);
-      uint32_t local = 0;
-      DkvItems it;
-      int32_t hq;
-      BlockRef br;
-      int half;
-      while (it.next(p, t, hq, br, half)) {
-        const uint32_t st = in_uses % kStages;
-        const uint32_t b2 = items & 1u;
-        if (!mbar_wait_warp(&s.in_full[st], (in_uses / kStages) & 1u, wc)) { ok = false; break; }
-        if (!mbar_wait_warp(&s.s_full[b2], (items >> 1) & 1u, wc)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t sv[64], dpv[64];
-        tmem_ld32(tmem + kColS + b2 * 64 + lane_off, sv);
-        tmem_ld32(tmem + kColS + b2 * 64 + 32 + lane_off, sv + 32);
-        tmem_ld32(tmem + kColDP + b2 * 64 + lane_off, dpv);
-        tmem_ld32(tmem + kColDP + b2 * 64 + 32 + lane_off, dpv + 32);
-        uint64_t allowed = ~0ull;
-        if (br.label == 1) {
-          if (p.mi.kind == BSA_MASK_DENSE) {
-            allowed = dense_bits_64(p.mi.partial + (static_cast<int64_t>(br.slot) * 128 + r) * 128 + half * 64);
-          } else {
-            const int64_t q0 = p.mi.q_sequence[br.col * 128 + half * 64];
-            allowed = interval_bits_64(q0, lo, hi);
-          }
+      if (!mbar_wait_warp(&s.st_full, n & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32(tmem + kDkvColST + col0 + lane_off, sv);
+      tmem_ld32(tmem + kDkvColST + col0 + 32 + lane_off, sv + 32);
+      uint64_t allowed = ~0ull;
+      if (label == 1) {
+        if (p.mi.kind == BSA_MASK_DENSE) {
+          allowed = dense_bits_64(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
+        } else {
+          const int64_t q0 = p.mi.q_sequence[col * 128 + col0];
+          allowed = interval_bits_64(q0, lo, hi);
         }
-        float lse2[64], dsc[64];
+      }
+      // per-column statistics of this half's 64 query rows
+      const float4* lse4 = reinterpret_cast<const float4*>(&s.lse[st][col0]);
+      tmem_wait_ld();
+      float pv[64];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          lse2[c] = s.lse[st][c] * kLog2e;
-          dsc[c] = s.dsum[st][c];
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = lse4[c4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c4 * 4 + e;
+          const float x = ex2_approx(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[e] * kLog2e));
+          pv[c] = ((allowed >> c) & 1ull) ? x : 0.f;
         }
+      }
+      uint32_t ppk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) ppk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+      tmem_st32(tmem + kDkvColST + col0 + lane_off, ppk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.p_full);
+      if (!mbar_wait_warp(&s.dpt_full, n & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      const float4* ds4 = reinterpret_cast<const float4*>(&s.dsum[st][col0]);
+      uint32_t dspk[32];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {  // 32 columns at a time to bound register use
+        uint32_t dpv[32];
+        tmem_ld32(tmem + kDkvColDP + col0 + h2 * 32 + lane_off, dpv);
         tmem_wait_ld();
-        uint32_t ppk[32], dspk[32];
-        p_ds_64<true>(sv, dpv, allowed, p.scale_log2, 0.f, 0.f, lse2, dsc, ppk, dspk);
-        tmem_st32(tmem + kColS + b2 * 64 + lane_off, ppk);
-        tmem_st32(tmem + kColDP + b2 * 64 + lane_off, dspk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&s.p_full[b2]);
-        ++in_uses;
-        ++items;
-        ++local;
-      }
-      if (!ok) break;
-      if (local > 0) {
-        if (!mbar_wait_warp(&s.acc_full, acc_uses & 1u, wc)) { ok = false; break; }
-        tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + colDV + c * 32 + lane_off, v);
-          tmem_wait_ld();
-          store_row(p.dv, p.grad_fp32, krow, D, v, c * 32, 1.f);
-          tmem_ld32(tmem + colDK + c * 32 + lane_off, v);
-          tmem_wait_ld();
-          store_row(p.dk, p.grad_fp32, krow, D, v, c * 32, p.scale);
-        }
-        tc_fence_before();
-        mbar_arrive(&s.acc_empty);
-        ++acc_uses;
-      } else {
-        store_zero_row(p.dk, p.grad_fp32, krow, D);
-        store_zero_row(p.dv, p.grad_fp32, krow, D);
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ===========================================================================
-// dQ
-// ===========================================================================
-template <int D>
-struct __align__(1024) DqSmem {
-  static constexpr int kTile = 128 * D * 2;
-  static constexpr int kHalf = 64 * D * 2;
-  uint8_t q[kTile];
-  uint8_t dout[kTile];
-  uint8_t k[kStages][kHalf];
-  uint8_t v[kStages][kHalf];
-  uint64_t qo_full, qo_empty;
-  uint64_t in_full[kStages], in_empty[kStages];
-  uint64_t s_full[2], p_full[2];
-  uint64_t acc_full, acc_empty, drain;
-  uint32_t tmem_base;
-  uint32_t abort_flag;
-};
-
-struct DqTile {
-  int32_t b, hq, i, hm, n;
-  int64_t row_base;
-};
-
-__device__ __forceinline__ DqTile dq_decode(const BwdParams& p, int32_t T) {
-  DqTile t;
-  if (p.mi.heads == 1) {
-    const int32_t bh = T % (p.B * p.Hq);
-    t.i = p.mi.row_order[T / (p.B * p.Hq)];
-    t.b = bh / p.Hq;
-    t.hq = bh % p.Hq;
-    t.hm = 0;
-  } else {
-    t.b = T % p.B;
-    const int32_t row = p.mi.row_order[T / p.B];
-    t.hm = row / p.mi.rows;
-    t.i = row % p.mi.rows;
-    t.hq = t.hm;
-  }
-  t.n = p.mi.row_len[t.hm * p.mi.rows + t.i];
-  t.row_base = (static_cast<int64_t>(t.hm) * p.mi.rows + t.i) * p.mi.width;
-  return t;
-}
-
-struct DqItems {
-  int half = 2;
-  Walk w;
-  BlockRef cur;
-  __device__ __forceinline__ bool next(const BwdParams& p, const DqTile& t, BlockRef& br, int& h) {
-    if (half >= 2) {
-      if (!w.next(p, t.row_base, t.n, cur)) return false;
-      half = 0;
-    }
-    br = cur;
-    h = half++;
-    return true;
-  }
-};
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const __grid_constant__ BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  using Smem = DqSmem<D>;
-  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kChunks = D / 64;
-  const int warp = warp_id();
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    s.abort_flag = 0;
-    mbar_init(&s.qo_full, 1);
-    mbar_init(&s.qo_empty, 1);
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.in_full[i], 1);
-      mbar_init(&s.in_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 128);
-    }
-    mbar_init(&s.acc_full, 1);
-    mbar_init(&s.acc_empty, 128);
-    mbar_init(&s.drain, 1);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&s.tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s.tmem_base;
-  const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
-
-  if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();
-      uint32_t qo_loads = 0, in_loads = 0;
-      bool ok = true;
-      for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
-        const DqTile t = dq_decode(p, T);
-        if (t.n == 0) continue;
-        if (qo_loads >= 1 && !mbar_wait(&s.qo_empty, (qo_loads - 1) & 1u, wc)) { ok = false; break; }
-        mbar_arrive_expect_tx(&s.qo_full, 2 * Smem::kTile);
-        const int32_t qrow = static_cast<int32_t>((static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + t.i * 128);
-        for (int c = 0; c < kChunks; ++c)
-          for (int rb = 0; rb < 2; ++rb) {
-            tma_load_2d(s.q + c * 16384 + rb * 8192, &tm_q, &s.qo_full, c * 64, qrow + rb * 64, pol_q);
-            tma_load_2d(s.dout + c * 16384 + rb * 8192, &tm_do, &s.qo_full, c * 64, qrow + rb * 64, pol_q);
-          }
-        ++qo_loads;
-        const int32_t g = t.hq / (p.Hq / p.Hkv);
-        const int64_t kv_base = (static_cast<int64_t>(t.b) * p.Hkv + g) * p.Skv;
-        DqItems it;
-        BlockRef br;
-        int half;
-        while (it.next(p, t, br, half)) {
-          const uint32_t st = in_loads % kStages;
-          if (in_loads >= kStages && !mbar_wait(&s.in_empty[st], ((in_loads / kStages) - 1) & 1u, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.in_full[st], 2 * Smem::kHalf);
-          const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128 + half * 64);
-          for (int c = 0; c < kChunks; ++c) {
-            tma_load_2d(s.k[st] + c * 8192, &tm_k, &s.in_full[st], c * 64, krow, pol_kv);
-            tma_load_2d(s.v[st] + c * 8192, &tm_v, &s.in_full[st], c * 64, krow, pol_kv);
-          }
-          ++in_loads;
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = ds4[h2 * 8 + c4];
+          const int c = h2 * 32 + c4 * 4, cl = c4 * 4;
+          dspk[c / 2] = pack_bf16x2(pv[c] * (__uint_as_float(dpv[cl]) - d4.x), pv[c + 1] * (__uint_as_float(dpv[cl + 1]) - d4.y));
+          dspk[c / 2 + 1] =
+              pack_bf16x2(pv[c + 2] * (__uint_as_float(dpv[cl + 2]) - d4.z), pv[c + 3] * (__uint_as_float(dpv[cl + 3]) - d4.w));
         }
       }
-      if (!ok) {
-        uint32_t dummy_abort = 0;
-        WaitCtl dw{nullptr, &dummy_abort, p.wait_ns};
-        if (qo_loads) (void)mbar_wait(&s.qo_full, (qo_loads - 1) & 1u, dw);
-        for (uint32_t i = (in_loads > kStages ? in_loads - kStages : 0); i < in_loads; ++i)
-          (void)mbar_wait(&s.in_full[i % kStages], (i / kStages) & 1u, dw);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
-      uint32_t qo_uses = 0, in_uses = 0, items = 0, acc_uses = 0, prev_stage = 0;
-      bool ok = true;
-      auto issue_acc = [&](uint32_t x, uint32_t stage, bool first) -> bool {
-        const uint32_t b2 = x & 1u;
-        if (!mbar_wait(&s.p_full[b2], (x >> 1) & 1u, wc)) return false;
-        if (first && acc_uses > 0 && !mbar_wait(&s.acc_empty, (acc_uses - 1) & 1u, wc)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(s.k[stage]);
+      tmem_st32(tmem + kDkvColDP + col0 + lane_off, dspk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.ds_full);
+      if (!last) continue;
+      if (!mbar_wait_warp(&s.acc_full, acc_uses & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + kColAcc, tmem + kColDP + b2 * 64 + kk * 8, sdesc_sw128(kb + kk * 2048, 8192, 1024), idesc_acc,
-                 (first && kk == 0) ? 0u : 1u);
-        mma_commit(&s.in_empty[stage]);
-        return true;
-      };
-      for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
-        const DqTile t = dq_decode(p, T);
-        if (t.n == 0) continue;
-        if (!mbar_wait(&s.qo_full, qo_uses & 1u, wc)) { ok = false; break; }
-        const uint32_t qb = smem_u32(s.q), dob = smem_u32(s.dout);
-        uint32_t local = 0;
-        DqItems it;
-        BlockRef br;
-        int half;
-        while (it.next(p, t, br, half)) {
-          const uint32_t st = in_uses % kStages;
-          if (!mbar_wait(&s.in_full[st], (in_uses / kStages) & 1u, wc)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t b2 = items & 1u;
-          const uint32_t kb = smem_u32(s.k[st]), vb = smem_u32(s.v[st]);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = (kk >> 2) * 8192 + (kk & 3) * 32;
-            mma_ss(tmem + kColS + b2 * 64, sdesc_sw128(qb + ao, 16, 1024), sdesc_sw128(kb + bo, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ao = (kk >> 2) * 16384 + (kk & 3) * 32, bo = (kk >> 2) * 8192 + (kk & 3) * 32;
-            mma_ss(tmem + kColDP + b2 * 64, sdesc_sw128(dob + ao, 16, 1024), sdesc_sw128(vb + bo, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&s.s_full[b2]);
-          if (local > 0 && !issue_acc(items - 1, prev_stage, local == 1)) { ok = false; break; }
-          prev_stage = st;
-          ++in_uses;
-          ++items;
-          ++local;
-        }
-        if (!ok) break;
-        mma_commit(&s.qo_empty);
-        ++qo_uses;
-        if (local > 0) {
-          if (!issue_acc(items - 1, prev_stage, local == 1)) { ok = false; break; }
-          mma_commit(&s.acc_full);
-          ++acc_uses;
-        }
-      }
-      mma_commit(&s.drain);
-      uint32_t dummy_abort = 0;
-      WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
-      (void)mbar_wait(&s.drain, 0, dw);
-    }
-  } else if (warp >= 4) {
-    const int r = static_cast<int>(threadIdx.x) - 128;  // query row in the tile == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t items = 0, acc_uses = 0;
-    bool ok = true;
-    for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
-      const DqTile t = dq_decode(p, T);
-      const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
-      if (t.n == 0) {
-        store_zero_row(p.dq, p.grad_fp32, qrow, D);
-        continue;
-      }
-      const float lse2 = p.lse[qrow] * kLog2e;
-      const float dsum_r = p.dsum[qrow];
-      int64_t lo = 0, hi = 0;
-      if (p.mi.kind != BSA_MASK_DENSE) {
-        const int64_t qi = p.mi.q_sequence[t.i * 128 + r];
-        key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, qi, lo, hi);
-      }
-      uint32_t local = 0;
-      DqItems it;
-      BlockRef br;
-      int half;
-      while (it.next(p, t, br, half)) {
-        const uint32_t b2 = items & 1u;
-        if (!mbar_wait_warp(&s.s_full[b2], (items >> 1) & 1u, wc)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t sv[64], dpv[64];
-        tmem_ld32(tmem + kColS + b2 * 64 + lane_off, sv);
-        tmem_ld32(tmem + kColS + b2 * 64 + 32 + lane_off, sv + 32);
-        tmem_ld32(tmem + kColDP + b2 * 64 + lane_off, dpv);
-        tmem_ld32(tmem + kColDP + b2 * 64 + 32 + lane_off, dpv + 32);
-        uint64_t allowed = ~0ull;
-        if (br.label == 1) {
-          if (p.mi.kind == BSA_MASK_DENSE)
-            allowed = dense_bits_64(p.mi.partial + (static_cast<int64_t>(br.slot) * 128 + r) * 128 + half * 64);
-          else
-            allowed = interval_bits_64(static_cast<int64_t>(br.col) * 128 + half * 64, lo, hi);
-        }
+      for (int c = 0; c < kHalfD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + kDkvColDV + half * kHalfD + c * 32 + lane_off, v);
         tmem_wait_ld();
-        uint32_t dspk[32];
-        p_ds_64<false>(sv, dpv, allowed, p.scale_log2, lse2, dsum_r, nullptr, nullptr, nullptr, dspk);
-        tmem_st32(tmem + kColDP + b2 * 64 + lane_off, dspk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&s.p_full[b2]);
-        ++items;
-        ++local;
+        store_row(p.dv, p.grad_fp32, krow, D, v, half * kHalfD + c * 32, 1.f);
+        tmem_ld32(tmem + kDkvColDK + half * kHalfD + c * 32 + lane_off, v);
+        tmem_wait_ld();
+        store_row(p.dk, p.grad_fp32, krow, D, v, half * kHalfD + c * 32, p.scale);
       }
-      if (!ok) break;
-      if (local > 0) {
-        if (!mbar_wait_warp(&s.acc_full, acc_uses & 1u, wc)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + kColAcc + c * 32 + lane_off, v);
-          tmem_wait_ld();
-          store_row(p.dq, p.grad_fp32, qrow, D, v, c * 32, p.scale);
-        }
-        tc_fence_before();
-        mbar_arrive(&s.acc_empty);
-        ++acc_uses;
-      } else {
-        store_zero_row(p.dq, p.grad_fp32, qrow, D);
-      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty);
+      ++acc_uses;
     }
   }
 
@@ -787,10 +923,10 @@ bool make_maps(const bsa_bwd_args* a, CUtensorMap* tq, CUtensorMap* tk, CUtensor
   const uint64_t q_rows = static_cast<uint64_t>(a->B) * a->Hq * a->S_q;
   const uint64_t kv_rows = static_cast<uint64_t>(a->B) * a->Hkv * a->S_kv;
   const int D = a->D;
-  return make_tmap_bf16_2d(tq, a->q, q_rows, D, D * 2, 64, 64) &&
-         make_tmap_bf16_2d(tk, a->k, kv_rows, D, D * 2, 64, 64) &&
-         make_tmap_bf16_2d(tv, a->v, kv_rows, D, D * 2, 64, 64) &&
-         make_tmap_bf16_2d(tdo, a->do_, q_rows, D, D * 2, 64, 64);
+  return make_tmap_bf16_2d(tq, a->q, q_rows, D, D * 2, 128, 64) &&
+         make_tmap_bf16_2d(tk, a->k, kv_rows, D, D * 2, 128, 64) &&
+         make_tmap_bf16_2d(tv, a->v, kv_rows, D, D * 2, 128, 64) &&
+         make_tmap_bf16_2d(tdo, a->do_, q_rows, D, D * 2, 128, 64);
 }
 
 BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float scale) {
