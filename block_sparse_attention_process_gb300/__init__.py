@@ -23,7 +23,7 @@ import torch
 from . import _abi
 from ._abi import BsaError, check
 
-__all__ = ["mask_compile", "MaskInfo", "fwd", "bwd", "bwd_rowsum", "bwd_dkv", "bwd_dq",
+__all__ = ["mask_compile", "MaskInfo", "fwd", "bwd", "bwd_noalloc", "bwd_rowsum", "bwd_dkv", "bwd_dq",
            "get_device_error", "set_wait_limit_ns", "debug_wait_timeout", "version", "BsaError",
            "library_path"]
 
@@ -199,6 +199,23 @@ def bwd(q, k, v, o, lse, do, fwd_info: MaskInfo, dkv_info: MaskInfo, *, dq=None,
     b = _bwd_args(q, k, v, o, lse, do, dq, dk, dv, dsum, softmax_scale, grad_fp32)
     check(_abi.lib().bsa_bwd(C.byref(b.args), fwd_info.handle, dkv_info.handle, _stream(stream)), "bsa_bwd")
     return b.dq, b.dk, b.dv
+
+
+def bwd_noalloc(q, k, v, o, lse, do, fwd_info: MaskInfo, dkv_info: MaskInfo, *, dq, dk, dv, softmax_scale=None,
+                grad_fp32: bool = False, stream=None):
+    """bsa_bwd_noalloc: the backward pass with no device allocation inside the
+    library (its rowsum scratch is a fixed 4 MiB device array); the caller
+    supplies the gradient buffers."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_bf16(n, t)
+    B, Hq, S, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    a = _abi.BwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                     None, B, Hq, Hkv, D, S, Skv, math.nan if softmax_scale is None else softmax_scale,
+                     1 if grad_fp32 else 0)
+    check(_abi.lib().bsa_bwd_noalloc(C.byref(a), fwd_info.handle, dkv_info.handle, _stream(stream)),
+          "bsa_bwd_noalloc")
+    return dq, dk, dv
 
 
 def bwd_rowsum(o, do, *, dsum=None, stream=None) -> torch.Tensor:

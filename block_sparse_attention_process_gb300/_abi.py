@@ -62,6 +62,7 @@ SIGNATURES = {
     "bsa_fwd": (C.c_int, [C.POINTER(FwdArgs), C.c_void_p, C.c_void_p]),
     "bsa_bwd": (C.c_int, [C.POINTER(BwdArgs), C.c_void_p, C.c_void_p, C.c_void_p]),
     "bsa_bwd_rowsum": (C.c_int, [C.POINTER(BwdArgs), C.c_void_p]),
+    "bsa_bwd_noalloc": (C.c_int, [C.POINTER(BwdArgs), C.c_void_p, C.c_void_p, C.c_void_p]),
     "bsa_bwd_dkv": (C.c_int, [C.POINTER(BwdArgs), C.c_void_p, C.c_void_p]),
     "bsa_bwd_dq": (C.c_int, [C.POINTER(BwdArgs), C.c_void_p, C.c_void_p]),
     "bsa_get_device_error": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint32)]),

@@ -929,7 +929,7 @@ bool make_maps(const bsa_bwd_args* a, CUtensorMap* tq, CUtensorMap* tk, CUtensor
          make_tmap_bf16_2d(tdo, a->do_, q_rows, D, D * 2, 128, 64);
 }
 
-BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float scale) {
+BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, uint32_t* err) {
   BwdParams p{};
   p.B = a->B;
   p.Hq = a->Hq;
@@ -947,16 +947,17 @@ BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
   p.dv = a->dv;
   p.grad_fp32 = a->grad_fp32 ? 1 : 0;
   p.mi = mask_info_dev(info);
-  p.err = device_error_word();
+  p.err = err ? err : device_error_word();
   p.wait_ns = wait_limit_ns();
   return p;
 }
 
 template <int D>
-bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream) {
+bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
+                      uint32_t* err) {
   CUtensorMap tq, tk, tv, tdo;
   if (!make_maps(a, &tq, &tk, &tv, &tdo)) return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor");
-  BwdParams p = make_params(a, info, scale);
+  BwdParams p = make_params(a, info, scale, err);
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
   p.n_tiles = a->B * a->Hkv * p.nK;
   const size_t smem = sizeof(DkvSmem<D>) + 1024;
@@ -974,10 +975,11 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
 }
 
 template <int D>
-bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream) {
+bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
+                     uint32_t* err) {
   CUtensorMap tq, tk, tv, tdo;
   if (!make_maps(a, &tq, &tk, &tv, &tdo)) return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor");
-  BwdParams p = make_params(a, info, scale);
+  BwdParams p = make_params(a, info, scale, err);
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
   p.n_tiles = a->B * a->Hq * p.nQ;
   const size_t smem = sizeof(DqSmem<D>) + 1024;
@@ -996,14 +998,16 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
 
 }  // namespace
 
-bsa_status dkv_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream) {
-  if (a->D == 128) return launch_dkv<128>(a, info, scale, stream);
-  return launch_dkv<64>(a, info, scale, stream);
+bsa_status dkv_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
+                      uint32_t* err) {
+  if (a->D == 128) return launch_dkv<128>(a, info, scale, stream, err);
+  return launch_dkv<64>(a, info, scale, stream, err);
 }
 
-bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream) {
-  if (a->D == 128) return launch_dq<128>(a, info, scale, stream);
-  return launch_dq<64>(a, info, scale, stream);
+bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
+                     uint32_t* err) {
+  if (a->D == 128) return launch_dq<128>(a, info, scale, stream, err);
+  return launch_dq<64>(a, info, scale, stream, err);
 }
 
 }  // namespace bsa

@@ -40,8 +40,11 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
                              bsa_mask_info** out);
 bsa_status fwd_launch(const bsa_fwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream);
 bsa_status rowsum_launch(const bsa_bwd_args* a, cudaStream_t stream);
-bsa_status dkv_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream);
-bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream);
+// `err` (optional) replaces the library's device error word for this launch.
+bsa_status dkv_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
+                      uint32_t* err = nullptr);
+bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
+                     uint32_t* err = nullptr);
 bsa_status debug_wait_timeout_launch(cudaStream_t stream);
 
 int num_sms();

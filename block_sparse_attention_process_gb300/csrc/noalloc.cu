@@ -1,0 +1,114 @@
+// bsa_bwd_noalloc: the backward pass without any device allocation.
+//
+// The ordinary backward needs two pieces of device memory besides its
+// inputs and outputs: the rowsum(dO*O) workspace (which the caller passes)
+// and the library's device error word (which the library allocates on the
+// first call on each device).  Here both live in file-scope device arrays
+// that exist from the moment the library is loaded on a device until the
+// process exits, so a call allocates and frees nothing.  The host only
+// needs their device addresses, which cudaGetSymbolAddress gives; that
+// set-up runs on the first call on each device, with that device current.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace bsa {
+namespace {
+
+// Largest B * Hq * S_q this entry point accepts (4 MiB of fp32 rowsum).
+constexpr int64_t kMaxRows = int64_t(1) << 20;
+
+// Shared by every call on a device; holds the last call's rowsum.
+static __device__ __align__(256) float g_dsum_scratch[kMaxRows];
+// Device-side error bits of this entry point's kernels (cleared by each call).
+static __device__ __align__(256) uint32_t g_err_scratch;
+
+std::mutex g_mu;
+float* g_dsum_ptr[64] = {nullptr};
+uint32_t* g_err_ptr[64] = {nullptr};
+
+// Device addresses of the two arrays for the current device.  In host code
+// the arrays' names are host-side stand-ins, not device addresses, so the
+// kernels are always given these resolved pointers.
+bsa_status resolve(float** dsum, uint32_t** err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(BSA_ERR_UNSUPPORTED, "device index above 63");
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_dsum_ptr[dev]) {
+    void* pd = nullptr;
+    void* pe = nullptr;
+    e = cudaGetSymbolAddress(&pd, g_dsum_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(rowsum scratch)");
+    e = cudaGetSymbolAddress(&pe, g_err_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    g_dsum_ptr[dev] = static_cast<float*>(pd);
+    g_err_ptr[dev] = static_cast<uint32_t*>(pe);
+  }
+  *dsum = g_dsum_ptr[dev];
+  *err = g_err_ptr[dev];
+  return BSA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bsa_status check(const bsa_bwd_args* a, const bsa_mask_info* fwd_info, const bsa_mask_info* dkv_info) {
+  if (!a) return fail(BSA_ERR_INVALID_ARG, "args is null");
+  if (a->B <= 0 || a->Hq <= 0 || a->Hkv <= 0) return fail(BSA_ERR_INVALID_ARG, "B, Hq and Hkv must be positive");
+  if (a->Hq % a->Hkv != 0) return fail(BSA_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+  if (a->S_q <= 0 || a->S_kv <= 0 || a->S_q % kBlock || a->S_kv % kBlock)
+    return fail(BSA_ERR_INVALID_ARG, "sequence lengths must be positive multiples of 128");
+  if (a->D != 64 && a->D != 128) return fail(BSA_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+  const int64_t rows = static_cast<int64_t>(a->B) * a->Hq * a->S_q;
+  if (rows > kMaxRows)
+    return fail(BSA_ERR_UNSUPPORTED, "bsa_bwd_noalloc: B*Hq*S_q = " + std::to_string(rows) +
+                                         " exceeds its fixed scratch of 1048576 rows; use bsa_bwd");
+  if (static_cast<int64_t>(a->B) * a->Hkv * a->S_kv > static_cast<int64_t>(INT32_MAX))
+    return fail(BSA_ERR_UNSUPPORTED, "B*Hkv*S_kv must fit in int32");
+  const void* ptrs[] = {a->q, a->k, a->v, a->o, a->lse, a->do_, a->dq, a->dk, a->dv};
+  for (const void* p : ptrs)
+    if (!p) return fail(BSA_ERR_INVALID_ARG, "a tensor pointer is null");
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(BSA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const bsa_mask_info* infos[2] = {fwd_info, dkv_info};
+  const int32_t orient[2] = {BSA_ORIENT_FWD, BSA_ORIENT_DKV};
+  for (int i = 0; i < 2; ++i) {
+    const bsa_mask_info* m = infos[i];
+    if (!m) return fail(BSA_ERR_INVALID_ARG, "MaskInfo is null");
+    if (m->orientation != orient[i]) return fail(BSA_ERR_INVALID_ARG, "MaskInfo has the wrong orientation");
+    if (m->q_len != a->S_q || m->kv_len != a->S_kv)
+      return fail(BSA_ERR_INVALID_ARG, "MaskInfo was compiled for other sequence lengths");
+    if (m->heads != 1 && m->heads != a->Hq) return fail(BSA_ERR_INVALID_ARG, "MaskInfo must have 1 or Hq mask heads");
+  }
+  return BSA_OK;
+}
+
+}  // namespace
+}  // namespace bsa
+
+using namespace bsa;
+
+extern "C" bsa_status bsa_bwd_noalloc(const bsa_bwd_args* a, const bsa_mask_info* fwd_info,
+                                      const bsa_mask_info* dkv_info, bsa_stream stream) {
+  bsa_status s = check(a, fwd_info, dkv_info);
+  if (s != BSA_OK) return s;
+  float* dsum = nullptr;
+  uint32_t* err = nullptr;
+  s = resolve(&dsum, &err);
+  if (s != BSA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  bsa_bwd_args b;
+  std::memcpy(&b, a, sizeof(b));
+  b.dsum = dsum;  // every row is rewritten by the rowsum kernel before it is read
+  const float scale = std::isnan(a->softmax_scale) ? 1.0f / std::sqrt(static_cast<float>(a->D)) : a->softmax_scale;
+  s = rowsum_launch(&b, st);
+  if (s != BSA_OK) return s;
+  s = dkv_launch(&b, dkv_info, scale, st, err);
+  if (s != BSA_OK) return s;
+  return dq_launch(&b, fwd_info, scale, st, err);
+}

@@ -181,6 +181,29 @@ BSA_API bsa_status bsa_bwd_dkv(const bsa_bwd_args* args, const bsa_mask_info* dk
 /* dQ: grid over (b, query head, query block), keys innermost. */
 BSA_API bsa_status bsa_bwd_dq(const bsa_bwd_args* args, const bsa_mask_info* fwd_info, bsa_stream stream);
 
+/* The backward pass (rowsum, dK/dV, dQ, same arguments and results as
+ * bsa_bwd) without allocating any device memory, for callers that cannot
+ * allocate: a runtime whose device memory is fixed up front by its own pool
+ * or budget, or a latency-critical loop that must not hit the device-wide
+ * synchronisation an allocation or free can cause.  The splash-attention
+ * pages have no counterpart; it is an addition of this library.
+ *   - args->dsum is ignored: the rowsum(dO*O) scratch is a file-scope device
+ *     array of 1,048,576 fp32 (4 MiB) that every GPU loading the library
+ *     holds until the process exits.  B * Hq * S_q above 1,048,576 is
+ *     rejected with BSA_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the array's device address for
+ *     that device (cudaGetSymbolAddress, with that device current); make
+ *     that first call before any stream capture.
+ *   - Every call shares the one array (and keeps the last call's rowsum in
+ *     it): calls that overlap on the GPU race, so serialise them (one
+ *     stream, or events).
+ *   - Device-side error bits of this entry point (a wait that ran out, a bad
+ *     MaskInfo index) go to a device word of its own, also static and
+ *     cleared at the start of each call; bsa_get_device_error does not
+ *     report them.  Host-side argument errors are returned as for bsa_bwd. */
+BSA_API bsa_status bsa_bwd_noalloc(const bsa_bwd_args* args, const bsa_mask_info* fwd_info,
+                                   const bsa_mask_info* dkv_info, bsa_stream stream);
+
 /* Synchronises `stream`, returns the device error word in *word (0 = none;
  * bit 1 = a bounded wait ran out, bit 2 = out-of-range MaskInfo index,
  * bit 4 = tensor-memory allocation failure) and clears it.  The status is
