@@ -51,6 +51,27 @@ def peaks():
     return {"bf16_tflops": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+KERNEL_NAMES = {"fwd": "fwd_kernel", "dkv": "dkv_kernel", "dq": "dq_kernel"}
+
+
+def traffic_per_launch(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu capture, or None when there
+    is no capture for this workload or the kernel source changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        ent = json.load(f).get(workload, {}).get(KERNEL_NAMES[kernel])
+    if not ent or not ent.get("valid"):
+        return None
+    src = os.path.join(ROOT, "block_sparse_attention_process_gb300", "csrc", ent["source"])
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != ent["source_sha"]:
+            return None
+    return ent["bytes_per_launch"]
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -216,14 +237,7 @@ def run_gpu(args):
     rowsum_bytes = 4 * w.B * w.Hq * w.S * w.D + 4 * w.B * w.Hq * w.S
     dom = max(kern, key=lambda k: kern[k]["ms"])
     achieved = kern[dom]["flop"] / (kern[dom]["ms"] * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            tj = json.load(f)
-        ent = tj.get(args.workload, {}).get(dom)
-        if ent and ent.get("valid", False):
-            traffic = ent["bytes_per_launch"]
+    traffic = traffic_per_launch(args.workload, dom)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
                 "peak_source": f"{pk['source']} bf16 burst"}
