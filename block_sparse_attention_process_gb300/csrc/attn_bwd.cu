@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s.tmem_base;
+  // broadcast from lane 0 so the compiler keeps it in a uniform register
+  const uint32_t tmem = __shfl_sync(0xffffffffu, s.tmem_base, 0);
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
 
   if (warp == 0) {
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_s = [&]() -> bool {  // S_n = Q K_n^T
       const uint32_t n = s_cnt;
       if (!k_ready(n)) return false;
-      const uint32_t info = s.binfo[n % kInfoRing].x;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[n % kInfoRing].x, 0);
       if ((info >> 20) & 1u) {  // first block of a tile: wait for its Q/dO
         if (!mbar_wait_warp(&s.qo_full, q_uses & 1u, wc)) return false;
         ++q_uses;
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_elect(&s.dp_full);
       mma_commit_elect(&s.v_empty[vs]);
-      const uint32_t info = s.binfo[n % kInfoRing].x;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[n % kInfoRing].x, 0);
       if ((info >> 21) & 1u) mma_commit_elect(&s.qo_empty);  // last S and dP of the tile are issued
       ++dp_cnt;
       return true;
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && total > 1) ok = issue_s();
     }
     for (uint32_t n = 0; ok && n < total; ++n) {
-      const uint32_t info = s.binfo[n % kInfoRing].x;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[n % kInfoRing].x, 0);
       const bool first = (info >> 20) & 1u, last = (info >> 21) & 1u;
       if (!mbar_wait_warp(&s.ds_full, n & 1u, wc)) { ok = false; break; }
       if (first && acc_uses > 0 && !mbar_wait_warp(&s.acc_empty, (acc_uses - 1) & 1u, wc)) { ok = false; break; }
@@ -678,7 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s.tmem_base;
+  // broadcast from lane 0 so the compiler keeps it in a uniform register
+  const uint32_t tmem = __shfl_sync(0xffffffffu, s.tmem_base, 0);
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
 
   if (warp == 0) {
@@ -752,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t n = 0; ok && n < total; ++n) {
       const uint32_t st = n % kDkvStages;
       if (!mbar_wait_warp(&s.in_full[st], (n / kDkvStages) & 1u, wc)) { ok = false; break; }
-      const uint32_t info = s.binfo[n % kInfoRing].x;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[n % kInfoRing].x, 0);
       const bool first = (info >> 20) & 1u, last = (info >> 21) & 1u;
       if (first) {
         if (!mbar_wait_warp(&s.kv_full, kv_uses & 1u, wc)) { ok = false; break; }

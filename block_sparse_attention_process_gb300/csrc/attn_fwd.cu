@@ -58,7 +58,9 @@ struct __align__(1024) FwdSmem {
   uint64_t v_full[kStagesV], v_empty[kStagesV];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t o_full, o_empty, drain;
-  uint4 binfo[kInfoRing];  // per block: {col | label<<16 | first<<20 | last<<21, slot, tile, 0}
+  // per block: {col | label<<16 | first<<20 | last<<21, stack slot, q_sequence of the tile's first
+  // query, (b*Hq + hq)*Sq + 128*i = output row of the tile's first query}
+  uint4 binfo[kInfoRing];
   float xmax[2][2][128];    // partial row maxima per [block parity][half][row]
   float xsum[2][128];       // partial row sums per [half][row] at the epilogue
   uint32_t tmem_base;
@@ -208,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s.tmem_base;
+  // broadcast from lane 0 so the compiler keeps it in a uniform register
+  const uint32_t tmem = __shfl_sync(0xffffffffu, s.tmem_base, 0);
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
 
   if (warp == 0) {
@@ -225,8 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       BlockRef br;
       bool first, last;
       int64_t kv_base = 0;
+      int32_t tile_q0 = 0;
+      uint32_t tile_row = 0;
       while (ok && sq.next(p, br, first, last)) {
         if (first) {
+          tile_q0 = p.mi.q_sequence[sq.t.i * 128];
+          tile_row = static_cast<uint32_t>((static_cast<int64_t>(sq.t.b) * p.Hq + sq.t.hq) * p.Sq + sq.t.i * 128);
           const uint32_t qb = q_loads & 1u;
           if (q_loads >= 2 && !mbar_wait(&s.q_empty[qb], ((q_loads >> 1) - 1) & 1u, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.q_full[qb], kTileBytes);
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s.binfo[k_loads % kInfoRing] =
             make_uint4(static_cast<uint32_t>(br.col) | (static_cast<uint32_t>(br.label) << 16) | (first ? 1u << 20 : 0u) |
                            (last ? 1u << 21 : 0u),
-                       static_cast<uint32_t>(br.slot), static_cast<uint32_t>(sq.T), 0u);
+                       static_cast<uint32_t>(br.slot), static_cast<uint32_t>(tile_q0), tile_row);
         mbar_arrive_expect_tx(&s.k_full[ks], kTileBytes);
         const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
         for (int c = 0; c < kChunks; ++c) tma_load_2d(s.k[ks] + c * 16384, &tm_k, &s.k_full[ks], c * 64, krow, pol_kv);
@@ -304,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_s = [&]() -> bool {
       const uint32_t ks = s_cnt % kStagesK;
       if (!mbar_wait_warp(&s.k_full[ks], (s_cnt / kStagesK) & 1u, wc)) return false;
-      const uint32_t info = s.binfo[s_cnt % kInfoRing].x;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[s_cnt % kInfoRing].x, 0);
       if (info & (1u << 20)) {  // first block of a tile: its Q buffer
         const uint32_t qb = q_uses & 1u;
         if (!mbar_wait_warp(&s.q_full[qb], (q_uses >> 1) & 1u, wc)) return false;
@@ -330,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     while (ok && s_cnt < total && s_cnt < static_cast<uint32_t>(kSBufs)) ok = issue_s();
     while (ok && pv_cnt < total) {
-      const uint32_t info = s.binfo[pv_cnt % kInfoRing].x;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[pv_cnt % kInfoRing].x, 0);
       const bool pv_first = (info >> 20) & 1u, pv_last = (info >> 21) & 1u;
       const uint32_t pb = pv_cnt % kSBufs;
       if (!mbar_wait_warp(&s.p_full[pb], (pv_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
@@ -389,7 +396,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f;  // l: this half's partial row sum
     int64_t lo = 0, hi = 0;
     uint32_t exec = 0;
-    Tile tt{};
+    // A finished tile's epilogue waits until the next tile's first block has
+    // been handed to the tensor cores, so the softmax never idles on the
+    // tile's last P V.
+    bool pending = false;
+    float pend_m = 0.f, pend_l = 0.f;
+    uint32_t pend_row = 0;
+    auto epilogue = [&]() -> bool {
+      s.xsum[half][r] = pend_l;
+      named_bar_sync(bar_id, 64);
+      const float l_row = pend_l + s.xsum[half ^ 1][r];
+      const int64_t orow = static_cast<int64_t>(pend_row) + r;
+      __nv_bfloat16* optr = p.o + orow * D + half * kOCols;
+      if (!mbar_wait_warp(&s.o_full, o_uses & 1u, wc)) return false;
+      tc_fence_after();
+      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
+#pragma unroll
+      for (int c = 0; c < kOCols / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tmem + ocol0 + c * 32 + lane_off, ov);
+        tmem_wait_ld();
+        uint4* dst = reinterpret_cast<uint4*>(optr + c * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 o4;
+          o4.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l);
+          o4.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l);
+          o4.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l);
+          o4.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l);
+          dst[v] = o4;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.o_empty);
+      ++o_uses;
+      if (half == 0) p.lse[orow] = l_row > 0.f ? (pend_m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+      pending = false;
+      return true;
+    };
     while (ok && s_cnt < total) {
       const uint32_t sb = s_cnt % kSBufs;
       if (!mbar_wait_warp(&s.s_full[sb], (s_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
@@ -399,14 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
-        tt = decode_tile(p, static_cast<int32_t>(bi.z));
         m = -INFINITY;
         l = 0.f;
         exec = 0;
-        if (p.mi.kind != BSA_MASK_DENSE) {
-          const int64_t q = p.mi.q_sequence[tt.i * 128 + r];
-          key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, q, lo, hi);
-        }
+        // q_sequence is consecutive within a query block: row r has q_sequence[128 i] + r
+        if (p.mi.kind != BSA_MASK_DENSE)
+          key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(static_cast<int32_t>(bi.z)) + r,
+                       lo, hi);
       }
       tc_fence_after();
       uint32_t xu[64];
@@ -532,39 +575,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&s.p_full[sb]);
       ++s_cnt;
       ++exec;
-      if (!last) continue;
-      // ---------------------------------------------------------- epilogue
-      s.xsum[half][r] = l;
-      named_bar_sync(bar_id, 64);
-      const float l_row = l + s.xsum[half ^ 1][r];
-      const int64_t orow = (static_cast<int64_t>(tt.b) * p.Hq + tt.hq) * p.Sq + static_cast<int64_t>(tt.i) * 128 + r;
-      __nv_bfloat16* optr = p.o + orow * D + half * kOCols;
-      if (!mbar_wait_warp(&s.o_full, o_uses & 1u, wc)) { ok = false; break; }
-      tc_fence_after();
-      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
-#pragma unroll
-      for (int c = 0; c < kOCols / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tmem + ocol0 + c * 32 + lane_off, ov);
-        tmem_wait_ld();
-        uint4* dst = reinterpret_cast<uint4*>(optr + c * 32);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 o4;
-          o4.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l);
-          o4.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l);
-          o4.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l);
-          o4.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l);
-          dst[v] = o4;
-        }
+      if (first && pending && !epilogue()) { ok = false; break; }
+      if (last) {
+        pending = true;
+        pend_m = (m == -INFINITY) ? 0.f : m;
+        pend_l = l;
+        pend_row = bi.w;
       }
-      tc_fence_before();
-      mbar_arrive(&s.o_empty);
-      ++o_uses;
-      if (half == 0) p.lse[orow] = l_row > 0.f ? (m_use + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
-      // the partner's read of xsum happens before its next write (next tile's epilogue)
-      // is reached, since both pass this tile's remaining exchange barriers in order
     }
+    if (ok && pending) ok = epilogue();
   }
 
   tc_fence_before();
