@@ -488,11 +488,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           allowed = interval_bits_64(static_cast<int64_t>(col) * 128 + col0, lo, hi);
       }
       tmem_wait_ld();
+      // P = exp2(s * scale_log2 - lse2), packed pairs
+      const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(-lse2, -lse2);
       float pv[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float e = ex2_approx(fmaf(__uint_as_float(sv[c]), scale_log2, -lse2));
-        pv[c] = ((allowed >> c) & 1ull) ? e : 0.f;
+      for (int c = 0; c < 64; c += 2) {
+        float e0, e1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl2), e0, e1);
+        pv[c] = ex2_approx(e0);
+        pv[c + 1] = ex2_approx(e1);
+      }
+      if (label == 1) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (!((allowed >> c) & 1ull)) pv[c] = 0.f;
       }
       if (!mbar_wait_warp(&s.dp_full, n & 1u, wc)) { ok = false; break; }
       tc_fence_after();
@@ -500,11 +509,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + kDqColDP + col0 + lane_off, dpv);
       tmem_ld32(tmem + kDqColDP + col0 + 32 + lane_off, dpv + 32);
       tmem_wait_ld();
+      // dS = P * (dP - Dsum)
+      const uint64_t nd2 = f2_pack(-dsum_r, -dsum_r);
       uint32_t dspk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        dspk[c] = pack_bf16x2(pv[2 * c] * (__uint_as_float(dpv[2 * c]) - dsum_r),
-                              pv[2 * c + 1] * (__uint_as_float(dpv[2 * c + 1]) - dsum_r));
+      for (int c = 0; c < 32; ++c) {
+        float d0, d1;
+        f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dpv[2 * c]), __uint_as_float(dpv[2 * c + 1])), nd2),
+                         f2_pack(pv[2 * c], pv[2 * c + 1])),
+                  d0, d1);
+        dspk[c] = pack_bf16x2(d0, d1);
+      }
       tmem_st32(tmem + kDqColDP + col0 + lane_off, dspk);
       tmem_wait_st();
       tc_fence_before();
@@ -853,17 +868,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       // per-column statistics of this half's 64 query rows
       const float4* lse4 = reinterpret_cast<const float4*>(&s.lse[st][col0]);
       tmem_wait_ld();
+      // P = exp2((s*scale - LSE) * log2e): (LSE - s*scale) then times -log2e, packed pairs
+      const uint64_t nsc2 = f2_pack(-p.scale, -p.scale), nl2e2 = f2_pack(-kLog2e, -kLog2e);
       float pv[64];
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l4 = lse4[c4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const int c = c4 * 4;
+        float e0, e1, e2, e3;
+        f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nsc2, f2_pack(l4.x, l4.y)),
+                         nl2e2),
+                  e0, e1);
+        f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), nsc2, f2_pack(l4.z, l4.w)),
+                         nl2e2),
+                  e2, e3);
+        pv[c] = ex2_approx(e0);
+        pv[c + 1] = ex2_approx(e1);
+        pv[c + 2] = ex2_approx(e2);
+        pv[c + 3] = ex2_approx(e3);
+      }
+      if (label == 1) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = c4 * 4 + e;
-          const float x = ex2_approx(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[e] * kLog2e));
-          pv[c] = ((allowed >> c) & 1ull) ? x : 0.f;
-        }
+        for (int c = 0; c < 64; ++c)
+          if (!((allowed >> c) & 1ull)) pv[c] = 0.f;
       }
       uint32_t ppk[32];
 #pragma unroll
@@ -885,9 +912,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = ds4[h2 * 8 + c4];
           const int c = h2 * 32 + c4 * 4, cl = c4 * 4;
-          dspk[c / 2] = pack_bf16x2(pv[c] * (__uint_as_float(dpv[cl]) - d4.x), pv[c + 1] * (__uint_as_float(dpv[cl + 1]) - d4.y));
-          dspk[c / 2 + 1] =
-              pack_bf16x2(pv[c + 2] * (__uint_as_float(dpv[cl + 2]) - d4.z), pv[c + 3] * (__uint_as_float(dpv[cl + 3]) - d4.w));
+          float a0, a1, a2, a3;
+          // dS = P * (dP - Dsum)
+          f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dpv[cl]), __uint_as_float(dpv[cl + 1])), f2_pack(-d4.x, -d4.y)),
+                           f2_pack(pv[c], pv[c + 1])),
+                    a0, a1);
+          f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dpv[cl + 2]), __uint_as_float(dpv[cl + 3])), f2_pack(-d4.z, -d4.w)),
+                           f2_pack(pv[c + 2], pv[c + 3])),
+                    a2, a3);
+          dspk[c / 2] = pack_bf16x2(a0, a1);
+          dspk[c / 2 + 1] = pack_bf16x2(a2, a3);
         }
       }
       tmem_st32(tmem + kDkvColDP + col0 + lane_off, dspk);

@@ -369,6 +369,18 @@ __device__ __forceinline__ uint32_t elect_one_lane() {
   return (threadIdx.x & 31u) == 0u;
 }
 
+// Register reconfiguration between warpgroups (all four warps of a
+// warpgroup execute the same instruction).  The launch's registers per
+// thread x threads bounds the sum over warpgroups.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
