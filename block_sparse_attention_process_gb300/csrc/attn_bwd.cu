@@ -57,6 +57,8 @@ struct BwdParams {
   void* dq;
   void* dk;
   void* dv;
+  const void* kp;  // K and V (for L2 prefetch)
+  const void* vp;
   int32_t grad_fp32;
   MaskInfoDev mi;
   int32_t n_tiles;
@@ -152,8 +154,11 @@ struct __align__(1024) DqSmem {
   uint64_t k_full[kDqStagesK], k_empty[kDqStagesK];
   uint64_t v_full[kDqStagesV], v_empty[kDqStagesV];
   uint64_t s_full[2], dp_full, ds_full;
-  uint64_t acc_full, acc_empty, drain;
-  uint4 binfo[kInfoRing];  // {col | label<<16 | first<<20 | last<<21, slot, tile, 0}
+  uint64_t acc_full, acc_empty, drain, stats_read;
+  // per block: {col | label<<16 | first<<20 | last<<21, stack slot, q_sequence of the tile's first
+  // query, (b*Hq + hq)*Sq + 128*i = row of the tile's first query}
+  uint4 binfo[kInfoRing];
+  float stats[2][128];  // LSE and Dsum of the tile's 128 query rows (loaded with Q and dO)
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -267,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, 256);
     mbar_init(&s.drain, 1);
+    mbar_init(&s.stats_read, 256);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
 
   if (warp == 0) {
-    // ------------------------------------------------ Q/dO (per tile) and K (per block); block ring
+    // ------------------------------------------------ Q/dO/LSE/Dsum (per tile) and K (per block); block ring
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -295,23 +301,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       BlockRef br;
       bool first, last;
       int64_t kv_base = 0;
+      int32_t tile_q0 = 0, qrow = 0;
       while (ok && sq.next(p, br, first, last)) {
         if (first) {
+          // the previous tile's Q/dO are free and its LSE/Dsum have been read
           if (qo_loads >= 1 && !mbar_wait(&s.qo_empty, (qo_loads - 1) & 1u, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.qo_full, 2 * kTile);
-          const int32_t qrow = static_cast<int32_t>((static_cast<int64_t>(sq.t.b) * p.Hq + sq.t.hq) * p.Sq + sq.t.i * 128);
+          if (qo_loads >= 1 && !mbar_wait(&s.stats_read, (qo_loads - 1) & 1u, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.qo_full, 2 * kTile + 1024);
+          qrow = static_cast<int32_t>((static_cast<int64_t>(sq.t.b) * p.Hq + sq.t.hq) * p.Sq + sq.t.i * 128);
+          tile_q0 = p.mi.q_sequence[sq.t.i * 128];
           for (int c = 0; c < kChunks; ++c) {
             tma_load_2d(s.q + c * 16384, &tm_q, &s.qo_full, c * 64, qrow, pol_q);
             tma_load_2d(s.dout + c * 16384, &tm_do, &s.qo_full, c * 64, qrow, pol_q);
           }
+          bulk_load(s.stats[0], p.lse + qrow, 512, &s.qo_full);
+          bulk_load(s.stats[1], p.dsum + qrow, 512, &s.qo_full);
           ++qo_loads;
           kv_base = (static_cast<int64_t>(sq.t.b) * p.Hkv + sq.t.hq / (p.Hq / p.Hkv)) * p.Skv;
         }
         const uint32_t ks = k_loads % kDqStagesK;
         if (k_loads >= kDqStagesK && !mbar_wait(&s.k_empty[ks], ((k_loads / kDqStagesK) - 1) & 1u, wc)) { ok = false; break; }
-        s.binfo[k_loads % kInfoRing] =
-            make_uint4(pack_info(br.col, br.label, first, last), static_cast<uint32_t>(br.slot),
-                       static_cast<uint32_t>(sq.T), 0u);
+        s.binfo[k_loads % kInfoRing] = make_uint4(pack_info(br.col, br.label, first, last), static_cast<uint32_t>(br.slot),
+                                                  static_cast<uint32_t>(tile_q0), static_cast<uint32_t>(qrow));
         mbar_arrive_expect_tx(&s.k_full[ks], kTile);
         const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
         for (int c = 0; c < kChunks; ++c) tma_load_2d(s.k[ks] + c * 16384, &tm_k, &s.k_full[ks], c * 64, krow, pol_kv);
@@ -459,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dq_decode(p, T).n);
     float lse2 = 0.f, dsum_r = 0.f;
     int64_t lo = 0, hi = 0, qrow = 0;
+    uint32_t tiles = 0;
     for (; ok && n < total; ++n) {
       const uint32_t sb = n & 1u;
       if (!mbar_wait_warp(&s.s_full[sb], (n >> 1) & 1u, wc)) { ok = false; break; }
@@ -467,14 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
-        const DqTile t = dq_decode(p, static_cast<int32_t>(bi.z));
-        qrow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
-        lse2 = p.lse[qrow] * kLog2e;
-        dsum_r = p.dsum[qrow];
-        if (p.mi.kind != BSA_MASK_DENSE) {
-          const int64_t qi = p.mi.q_sequence[t.i * 128 + r];
-          key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, qi, lo, hi);
-        }
+        // row statistics arrive with the tile's Q/dO; q_sequence is consecutive within a block
+        qrow = static_cast<int64_t>(bi.w) + r;
+        if (p.mi.kind != BSA_MASK_DENSE)
+          key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(static_cast<int32_t>(bi.z)) + r,
+                       lo, hi);
+        if (!mbar_wait_warp(&s.qo_full, tiles & 1u, wc)) { ok = false; break; }
+        lse2 = s.stats[0][r] * kLog2e;
+        dsum_r = s.stats[1][r];
+        mbar_arrive(&s.stats_read);
+        ++tiles;
       }
       tc_fence_after();
       uint32_t sv[64];
@@ -570,7 +584,9 @@ struct __align__(1024) DkvSmem {
   uint64_t in_full[kDkvStages], in_empty[kDkvStages];
   uint64_t st_full, dpt_full, p_full, ds_full;
   uint64_t acc_full, acc_empty, drain;
-  uint4 binfo[kInfoRing];  // {col | label<<16 | first<<20 | last<<21, slot, tile, q head}
+  // per item: {col | label<<16 | first<<20 | last<<21, stack slot (dense) or q_sequence of the
+  // query block's first row (computable), 128*j = first key of the tile, row of that key in dK/dV}
+  uint4 binfo[kInfoRing];
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -720,6 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(s.v + c * 16384, &tm_v, &s.kv_full, c * 64, krow, pol_kv);
         }
         ++kv_loads;
+        // warm L2 with this CTA's next tile's K and V
+        for (int32_t T2 = T + static_cast<int32_t>(gridDim.x); T2 < p.n_tiles; T2 += gridDim.x) {
+          const DkvTile t2 = dkv_decode(p, T2);
+          if (t2.total == 0) continue;
+          const int64_t row2 = (static_cast<int64_t>(t2.b) * p.Hkv + t2.g) * p.Skv + t2.j * 128;
+          prefetch_l2(static_cast<const uint8_t*>(p.kp) + row2 * D * 2, 128 * D * 2);
+          prefetch_l2(static_cast<const uint8_t*>(p.vp) + row2 * D * 2, 128 * D * 2);
+          break;
+        }
         DkvItems it;
         it.init(p, t);
         int32_t hq;
@@ -728,9 +753,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           it.next(p, t, hq, br);
           const uint32_t st = in_loads % kDkvStages;
           if (in_loads >= kDkvStages && !mbar_wait(&s.in_empty[st], ((in_loads / kDkvStages) - 1) & 1u, wc)) { ok = false; break; }
-          s.binfo[in_loads % kInfoRing] = make_uint4(pack_info(br.col, br.label, x == 0, x == t.total - 1),
-                                                     static_cast<uint32_t>(br.slot), static_cast<uint32_t>(T),
-                                                     static_cast<uint32_t>(hq));
+          const uint32_t extra = p.mi.kind == BSA_MASK_DENSE ? static_cast<uint32_t>(br.slot)
+                                                             : static_cast<uint32_t>(p.mi.q_sequence[br.col * 128]);
+          s.binfo[in_loads % kInfoRing] = make_uint4(pack_info(br.col, br.label, x == 0, x == t.total - 1), extra,
+                                                     static_cast<uint32_t>(t.j * 128), static_cast<uint32_t>(krow));
           mbar_arrive_expect_tx(&s.in_full[st], 2 * kTile + 1024);
           const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + hq) * p.Sq + br.col * 128;
           for (int c = 0; c < kChunks; ++c) {
@@ -846,10 +872,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
-        const DkvTile t = dkv_decode(p, static_cast<int32_t>(bi.z));
-        krow = (static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + static_cast<int64_t>(t.j) * 128 + r;
+        krow = static_cast<int64_t>(bi.w) + r;
         if (p.mi.kind != BSA_MASK_DENSE)
-          query_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(t.j) * 128 + r, lo, hi);
+          query_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(bi.z) + r, lo, hi);
       }
       if (!mbar_wait_warp(&s.st_full, n & 1u, wc)) { ok = false; break; }
       tc_fence_after();
@@ -861,8 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.mi.kind == BSA_MASK_DENSE) {
           allowed = dense_bits_64(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
         } else {
-          const int64_t q0 = p.mi.q_sequence[col * 128 + col0];
-          allowed = interval_bits_64(q0, lo, hi);
+          // q_sequence is consecutive within a query block
+          allowed = interval_bits_64(static_cast<int64_t>(static_cast<int32_t>(bi.y)) + col0, lo, hi);
         }
       }
       // per-column statistics of this half's 64 query rows
@@ -981,6 +1006,8 @@ BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
   p.dq = a->dq;
   p.dk = a->dk;
   p.dv = a->dv;
+  p.kp = a->k;
+  p.vp = a->v;
   p.grad_fp32 = a->grad_fp32 ? 1 : 0;
   p.mi = mask_info_dev(info);
   p.err = err ? err : device_error_word();
