@@ -43,7 +43,17 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;  // dQ launch: 4 role warps + 8 elementwise warps
+
+// dK/dV launch: the elementwise work is split over kDkvParts warpgroups, each
+// taking 128 / kDkvParts of the query columns (and D / kDkvParts of the
+// output columns at the epilogue).
+template <int D>
+struct DkvShape {
+  static constexpr int kParts = D == 128 ? 4 : 2;
+  static constexpr int kCols = 128 / kParts;
+  static constexpr int kThreads = 128 + 128 * kParts;
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr int kInfoRing = 16;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -102,6 +112,38 @@ __device__ __forceinline__ void store_zero_cols(void* base, int fp32, int64_t ro
     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + row * D + c0);
     for (int e = 0; e < n / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
   }
+}
+
+// TMEM column of 16-bit A-operand k-step kk when the operand is split into
+// parts of kCols columns, each part's kCols/2 packed words at the start of
+// its own kCols-column range.
+template <int kCols>
+__device__ __forceinline__ uint32_t part_a_col(int kk) {
+  constexpr int kSteps = kCols / 16;  // k-steps (16 elements = 8 columns) per part
+  return static_cast<uint32_t>((kk / kSteps) * kCols + (kk % kSteps) * 8);
+}
+
+// Store N (16 or 32) consecutive TMEM columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
+  if constexpr (N == 32) tmem_st32(taddr, r);
+  else tmem_st16(taddr, r);
+}
+
+// Visibility bits of N (32 or 64) consecutive columns of one row of a stacked block.
+template <int N>
+__device__ __forceinline__ uint64_t dense_bits(const uint8_t* row) {
+  uint64_t bits = 0;
+  const uint4* src = reinterpret_cast<const uint4*>(row);
+#pragma unroll
+  for (int v = 0; v < N / 16; ++v) {
+    const uint4 w = __ldg(src + v);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if ((wv[e >> 2] >> ((e & 3) * 8)) & 0xFFu) bits |= 1ull << (v * 16 + e);
+  }
+  return bits;
 }
 
 // Visibility bits of 64 consecutive columns of one row of a stacked block.
@@ -674,7 +716,7 @@ struct DkvItems {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ BwdParams p) {
@@ -696,10 +738,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&s.st_full, 1);
     mbar_init(&s.dpt_full, 1);
-    mbar_init(&s.p_full, 256);
-    mbar_init(&s.ds_full, 256);
+    mbar_init(&s.p_full, 128 * DkvShape<D>::kParts);
+    mbar_init(&s.ds_full, 128 * DkvShape<D>::kParts);
     mbar_init(&s.acc_full, 1);
-    mbar_init(&s.acc_empty, 256);
+    mbar_init(&s.acc_empty, 128 * DkvShape<D>::kParts);
     mbar_init(&s.drain, 1);
     fence_mbar_init();
   }
@@ -823,7 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t domn = domn0 + st * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_elect(tmem + kDkvColDV, tmem + kDkvColST + split_a_col(kk), domn + static_cast<uint64_t>(kk * 2048 >> 4),
+        mma_ts_elect(tmem + kDkvColDV, tmem + kDkvColST + part_a_col<DkvShape<D>::kCols>(kk),
+                     domn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
       // dK += dS^T Q
       if (!mbar_wait_warp(&s.ds_full, n & 1u, wc)) { ok = false; break; }
@@ -831,7 +874,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qmn = qmn0 + st * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_elect(tmem + kDkvColDK, tmem + kDkvColDP + split_a_col(kk), qmn + static_cast<uint64_t>(kk * 2048 >> 4),
+        mma_ts_elect(tmem + kDkvColDK, tmem + kDkvColDP + part_a_col<DkvShape<D>::kCols>(kk),
+                     qmn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
       mma_commit_elect(&s.in_empty[st]);
       if (last) {
@@ -844,31 +888,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
     (void)mbar_wait(&s.drain, 0, dw);
   } else if (warp >= 4) {
-    // ------------------------------------------------ P^T and dS^T (two warpgroups)
-    const int half = (warp - 4) >> 2;
+    // ------------------------------------------------ P^T and dS^T (kParts warpgroups)
+    constexpr int kParts = DkvShape<D>::kParts;
+    constexpr int kCols = DkvShape<D>::kCols;  // query columns per thread
+    constexpr int kPartD = D / kParts;         // output columns per thread at the epilogue
+    const int part = (warp - 4) >> 2;
     const int quarter = (warp - 4) & 3;
     const int r = quarter * 32 + lane;  // key row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t col0 = static_cast<uint32_t>(half) * 64;  // query columns of this half
-    constexpr int kHalfD = D / 2;
-    const float scale_log2 = p.scale_log2;
+    const uint32_t col0 = static_cast<uint32_t>(part) * kCols;  // query columns of this part
     bool ok = true;
     for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) {
       const DkvTile t = dkv_decode(p, T);
       if (t.total > 0) continue;
       const int64_t krow = (static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + static_cast<int64_t>(t.j) * 128 + r;
-      store_zero_cols(p.dk, p.grad_fp32, krow, D, half * kHalfD, kHalfD);
-      store_zero_cols(p.dv, p.grad_fp32, krow, D, half * kHalfD, kHalfD);
+      store_zero_cols(p.dk, p.grad_fp32, krow, D, part * kPartD, kPartD);
+      store_zero_cols(p.dv, p.grad_fp32, krow, D, part * kPartD, kPartD);
     }
     uint32_t total = 0;
     for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dkv_decode(p, T).total);
     uint32_t acc_uses = 0;
     int64_t lo = 0, hi = 0, krow = 0;
+    const uint64_t nsc2 = f2_pack(-p.scale, -p.scale), nl2e2 = f2_pack(-kLog2e, -kLog2e);
     for (uint32_t n = 0; ok && n < total; ++n) {
       const uint32_t st = n % kDkvStages;
       if (!mbar_wait_warp(&s.in_full[st], (n / kDkvStages) & 1u, wc)) { ok = false; break; }
       const uint4 bi = s.binfo[n % kInfoRing];
-      const int32_t col = static_cast<int32_t>(bi.x & 0xFFFFu);
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
@@ -878,26 +923,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!mbar_wait_warp(&s.st_full, n & 1u, wc)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[64];
-      tmem_ld32(tmem + kDkvColST + col0 + lane_off, sv);
-      tmem_ld32(tmem + kDkvColST + col0 + 32 + lane_off, sv + 32);
+      uint32_t sv[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDkvColST + col0 + c + lane_off, sv + c);
       uint64_t allowed = ~0ull;
       if (label == 1) {
         if (p.mi.kind == BSA_MASK_DENSE) {
-          allowed = dense_bits_64(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
+          allowed = dense_bits<kCols>(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
         } else {
           // q_sequence is consecutive within a query block
           allowed = interval_bits_64(static_cast<int64_t>(static_cast<int32_t>(bi.y)) + col0, lo, hi);
         }
       }
-      // per-column statistics of this half's 64 query rows
+      // per-column statistics of this part's query rows
       const float4* lse4 = reinterpret_cast<const float4*>(&s.lse[st][col0]);
       tmem_wait_ld();
       // P = exp2((s*scale - LSE) * log2e): (LSE - s*scale) then times -log2e, packed pairs
-      const uint64_t nsc2 = f2_pack(-p.scale, -p.scale), nl2e2 = f2_pack(-kLog2e, -kLog2e);
-      float pv[64];
+      float pv[kCols];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
+      for (int c4 = 0; c4 < kCols / 4; ++c4) {
         const float4 l4 = lse4[c4];
         const int c = c4 * 4;
         float e0, e1, e2, e3;
@@ -914,22 +958,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (label == 1) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kCols; ++c)
           if (!((allowed >> c) & 1ull)) pv[c] = 0.f;
       }
-      uint32_t ppk[32];
+      {
+        uint32_t ppk[kCols / 2];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) ppk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-      tmem_st32(tmem + kDkvColST + col0 + lane_off, ppk);
+        for (int c = 0; c < kCols / 2; ++c) ppk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+        tmem_st_cols<kCols / 2>(tmem + kDkvColST + col0 + lane_off, ppk);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.p_full);
       if (!mbar_wait_warp(&s.dpt_full, n & 1u, wc)) { ok = false; break; }
       tc_fence_after();
       const float4* ds4 = reinterpret_cast<const float4*>(&s.dsum[st][col0]);
-      uint32_t dspk[32];
+      uint32_t dspk[kCols / 2];
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {  // 32 columns at a time to bound register use
+      for (int h2 = 0; h2 < kCols / 32; ++h2) {  // 32 columns at a time to bound register use
         uint32_t dpv[32];
         tmem_ld32(tmem + kDkvColDP + col0 + h2 * 32 + lane_off, dpv);
         tmem_wait_ld();
@@ -949,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dspk[c / 2 + 1] = pack_bf16x2(a2, a3);
         }
       }
-      tmem_st32(tmem + kDkvColDP + col0 + lane_off, dspk);
+      tmem_st_cols<kCols / 2>(tmem + kDkvColDP + col0 + lane_off, dspk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.ds_full);
@@ -957,14 +1003,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(&s.acc_full, acc_uses & 1u, wc)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kHalfD / 32; ++c) {
+      for (int c = 0; c < kPartD / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + kDkvColDV + half * kHalfD + c * 32 + lane_off, v);
+        tmem_ld32(tmem + kDkvColDV + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
-        store_row(p.dv, p.grad_fp32, krow, D, v, half * kHalfD + c * 32, 1.f);
-        tmem_ld32(tmem + kDkvColDK + half * kHalfD + c * 32 + lane_off, v);
+        store_row(p.dv, p.grad_fp32, krow, D, v, part * kPartD + c * 32, 1.f);
+        tmem_ld32(tmem + kDkvColDK + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
-        store_row(p.dk, p.grad_fp32, krow, D, v, half * kHalfD + c * 32, p.scale);
+        store_row(p.dk, p.grad_fp32, krow, D, v, part * kPartD + c * 32, p.scale);
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty);
@@ -1031,7 +1077,7 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  dkv_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  dkv_kernel<D><<<grid, DkvShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dkv launch");
   return BSA_OK;
