@@ -43,17 +43,20 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 384;  // dQ launch: 4 role warps + 8 elementwise warps
-
-// dK/dV launch: the elementwise work is split over kDkvParts warpgroups, each
-// taking 128 / kDkvParts of the query columns (and D / kDkvParts of the
-// output columns at the epilogue).
+// Both gradient launches split their elementwise work over kParts
+// warpgroups, each taking 128 / kParts of the score columns (and D / kParts
+// of the output columns at the epilogue), beside one warpgroup of role
+// warps (producers, MMA issuer).
 template <int D>
-struct DkvShape {
+struct EwShape {
   static constexpr int kParts = D == 128 ? 4 : 2;
   static constexpr int kCols = 128 / kParts;
   static constexpr int kThreads = 128 + 128 * kParts;
 };
+template <int D>
+using DkvShape = EwShape<D>;
+template <int D>
+using DqShape = EwShape<D>;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kInfoRing = 16;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -75,11 +78,6 @@ struct BwdParams {
   uint32_t* err;
   uint64_t wait_ns;
 };
-
-// TMEM column of 16-bit A-operand k-step kk (16 elements = 8 columns) when
-// the two halves of a 128-wide operand sit at columns [0, 32) and [64, 96)
-// of a 128-column buffer.
-__device__ __forceinline__ uint32_t split_a_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
 __device__ __forceinline__ void store_row(void* base, int fp32, int64_t row, int D, const uint32_t* v, int c0,
                                           float mul) {
@@ -137,21 +135,6 @@ __device__ __forceinline__ uint64_t dense_bits(const uint8_t* row) {
   const uint4* src = reinterpret_cast<const uint4*>(row);
 #pragma unroll
   for (int v = 0; v < N / 16; ++v) {
-    const uint4 w = __ldg(src + v);
-    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-      if ((wv[e >> 2] >> ((e & 3) * 8)) & 0xFFu) bits |= 1ull << (v * 16 + e);
-  }
-  return bits;
-}
-
-// Visibility bits of 64 consecutive columns of one row of a stacked block.
-__device__ __forceinline__ uint64_t dense_bits_64(const uint8_t* row64) {
-  uint64_t bits = 0;
-  const uint4* src = reinterpret_cast<const uint4*>(row64);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
     const uint4 w = __ldg(src + v);
     const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -283,7 +266,7 @@ struct DqSeq {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ BwdParams p) {
@@ -310,11 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.s_full[0], 1);
     mbar_init(&s.s_full[1], 1);
     mbar_init(&s.dp_full, 1);
-    mbar_init(&s.ds_full, 256);
+    mbar_init(&s.ds_full, 128 * DqShape<D>::kParts);
     mbar_init(&s.acc_full, 1);
-    mbar_init(&s.acc_empty, 256);
+    mbar_init(&s.acc_empty, 128 * DqShape<D>::kParts);
     mbar_init(&s.drain, 1);
-    mbar_init(&s.stats_read, 256);
+    mbar_init(&s.stats_read, 128 * DqShape<D>::kParts);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -477,7 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t kmn = kmn0 + (n % kDqStagesK) * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_elect(tmem + kDqColQ, tmem + kDqColDP + split_a_col(kk), kmn + static_cast<uint64_t>(kk * 2048 >> 4),
+        mma_ts_elect(tmem + kDqColQ, tmem + kDqColDP + part_a_col<DqShape<D>::kCols>(kk),
+                     kmn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
       mma_commit_elect(&s.k_empty[n % kDqStagesK]);
       if (last) {
@@ -492,13 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
     (void)mbar_wait(&s.drain, 0, dw);
   } else if (warp >= 4) {
-    // ------------------------------------------------ P and dS (two warpgroups)
-    const int half = (warp - 4) >> 2;
+    // ------------------------------------------------ P and dS (kParts warpgroups)
+    constexpr int kParts = DqShape<D>::kParts;
+    constexpr int kCols = DqShape<D>::kCols;  // key columns per thread
+    constexpr int kPartD = D / kParts;        // dQ columns per thread at the epilogue
+    const int part = (warp - 4) >> 2;
     const int quarter = (warp - 4) & 3;
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t col0 = static_cast<uint32_t>(half) * 64;
-    constexpr int kHalfD = D / 2;
+    const uint32_t col0 = static_cast<uint32_t>(part) * kCols;
     const float scale_log2 = p.scale_log2;
     uint32_t n = 0, acc_uses = 0;
     bool ok = true;
@@ -506,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const DqTile t = dq_decode(p, T);
       if (t.n > 0) continue;
       const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
-      store_zero_cols(p.dq, p.grad_fp32, qrow, D, half * kHalfD, kHalfD);
+      store_zero_cols(p.dq, p.grad_fp32, qrow, D, part * kPartD, kPartD);
     }
     uint32_t total = 0;
     for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dq_decode(p, T).n);
@@ -533,22 +519,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++tiles;
       }
       tc_fence_after();
-      uint32_t sv[64];
-      tmem_ld32(tmem + kDqColS + sb * 128 + col0 + lane_off, sv);
-      tmem_ld32(tmem + kDqColS + sb * 128 + col0 + 32 + lane_off, sv + 32);
+      uint32_t sv[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDqColS + sb * 128 + col0 + c + lane_off, sv + c);
       uint64_t allowed = ~0ull;
       if (label == 1) {
         if (p.mi.kind == BSA_MASK_DENSE)
-          allowed = dense_bits_64(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
+          allowed = dense_bits<kCols>(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
         else
           allowed = interval_bits_64(static_cast<int64_t>(col) * 128 + col0, lo, hi);
       }
       tmem_wait_ld();
       // P = exp2(s * scale_log2 - lse2), packed pairs
       const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(-lse2, -lse2);
-      float pv[64];
+      float pv[kCols];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
+      for (int c = 0; c < kCols; c += 2) {
         float e0, e1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl2), e0, e1);
         pv[c] = ex2_approx(e0);
@@ -556,27 +542,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (label == 1) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kCols; ++c)
           if (!((allowed >> c) & 1ull)) pv[c] = 0.f;
       }
       if (!mbar_wait_warp(&s.dp_full, n & 1u, wc)) { ok = false; break; }
       tc_fence_after();
-      uint32_t dpv[64];
-      tmem_ld32(tmem + kDqColDP + col0 + lane_off, dpv);
-      tmem_ld32(tmem + kDqColDP + col0 + 32 + lane_off, dpv + 32);
+      uint32_t dpv[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDqColDP + col0 + c + lane_off, dpv + c);
       tmem_wait_ld();
       // dS = P * (dP - Dsum)
       const uint64_t nd2 = f2_pack(-dsum_r, -dsum_r);
-      uint32_t dspk[32];
+      uint32_t dspk[kCols / 2];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < kCols / 2; ++c) {
         float d0, d1;
         f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dpv[2 * c]), __uint_as_float(dpv[2 * c + 1])), nd2),
                          f2_pack(pv[2 * c], pv[2 * c + 1])),
                   d0, d1);
         dspk[c] = pack_bf16x2(d0, d1);
       }
-      tmem_st32(tmem + kDqColDP + col0 + lane_off, dspk);
+      tmem_st_cols<kCols / 2>(tmem + kDqColDP + col0 + lane_off, dspk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.ds_full);
@@ -584,11 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(&s.acc_full, acc_uses & 1u, wc)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kHalfD / 32; ++c) {
+      for (int c = 0; c < kPartD / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + kDqColQ + half * kHalfD + c * 32 + lane_off, v);
+        tmem_ld32(tmem + kDqColQ + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
-        store_row(p.dq, p.grad_fp32, qrow, D, v, half * kHalfD + c * 32, p.scale);
+        store_row(p.dq, p.grad_fp32, qrow, D, v, part * kPartD + c * 32, p.scale);
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty);
@@ -1099,7 +1085,7 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  dq_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  dq_kernel<D><<<grid, DqShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dq launch");
   return BSA_OK;
