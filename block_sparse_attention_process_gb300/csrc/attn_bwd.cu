@@ -518,10 +518,6 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
         mbar_arrive(&s.stats_read);
         ++tiles;
       }
-      tc_fence_after();
-      uint32_t sv[kCols];
-#pragma unroll
-      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDqColS + sb * 128 + col0 + c + lane_off, sv + c);
       uint64_t allowed = ~0ull;
       if (label == 1) {
         if (p.mi.kind == BSA_MASK_DENSE)
@@ -529,7 +525,13 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
         else
           allowed = interval_bits_64(static_cast<int64_t>(col) * 128 + col0, lo, hi);
       }
+      // no branch joins while the loaded registers are in flight
+      tc_fence_after();
+      uint32_t sv[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDqColS + sb * 128 + col0 + c + lane_off, sv + c);
       tmem_wait_ld();
+      reg_fence<kCols>(sv);
       // P = exp2(s * scale_log2 - lse2), packed pairs
       const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(-lse2, -lse2);
       float pv[kCols];
@@ -551,6 +553,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDqColDP + col0 + c + lane_off, dpv + c);
       tmem_wait_ld();
+      reg_fence<kCols>(dpv);
       // dS = P * (dP - Dsum)
       const uint64_t nd2 = f2_pack(-dsum_r, -dsum_r);
       uint32_t dspk[kCols / 2];
@@ -574,6 +577,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + kDqColQ + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
+        reg_fence32(v);
         store_row(p.dq, p.grad_fp32, qrow, D, v, part * kPartD + c * 32, p.scale);
       }
       tc_fence_before();
@@ -908,10 +912,6 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           query_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(bi.z) + r, lo, hi);
       }
       if (!mbar_wait_warp(&s.st_full, n & 1u, wc)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sv[kCols];
-#pragma unroll
-      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDkvColST + col0 + c + lane_off, sv + c);
       uint64_t allowed = ~0ull;
       if (label == 1) {
         if (p.mi.kind == BSA_MASK_DENSE) {
@@ -923,7 +923,13 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       }
       // per-column statistics of this part's query rows
       const float4* lse4 = reinterpret_cast<const float4*>(&s.lse[st][col0]);
+      // no branch joins while the loaded registers are in flight
+      tc_fence_after();
+      uint32_t sv[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDkvColST + col0 + c + lane_off, sv + c);
       tmem_wait_ld();
+      reg_fence<kCols>(sv);
       // P = exp2((s*scale - LSE) * log2e): (LSE - s*scale) then times -log2e, packed pairs
       float pv[kCols];
 #pragma unroll
@@ -965,6 +971,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         uint32_t dpv[32];
         tmem_ld32(tmem + kDkvColDP + col0 + h2 * 32 + lane_off, dpv);
         tmem_wait_ld();
+        reg_fence32(dpv);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = ds4[h2 * 8 + c4];
@@ -993,9 +1000,11 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + kDkvColDV + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
+        reg_fence32(v);
         store_row(p.dv, p.grad_fp32, krow, D, v, part * kPartD + c * 32, 1.f);
         tmem_ld32(tmem + kDkvColDK + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
+        reg_fence32(v);
         store_row(p.dk, p.grad_fp32, krow, D, v, part * kPartD + c * 32, p.scale);
       }
       tc_fence_before();

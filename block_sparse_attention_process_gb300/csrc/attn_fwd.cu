@@ -41,8 +41,17 @@ namespace {
 constexpr int kStagesK = 2;
 constexpr int kStagesV = 2;
 constexpr int kSBufs = 3;         // score buffers in TMEM
-constexpr int kInfoRing = 16;     // block descriptors published by the K producer
-constexpr int kThreads = 384;  // 4 role warps + 8 softmax warps
+constexpr int kInfoRing = 32;     // block descriptors published by the walker warp
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = 128 + 32 * kSoftmaxWarps;  // 4 role warps + the softmax warps
+// Readers that release a block descriptor: the V producer and every softmax
+// warp.  A softmax warp releases it once the block's scores are ready, by
+// when the K producer and the MMA warp have read it too.
+constexpr uint32_t kInfoReaders = 1 + kSoftmaxWarps;
+// Flags in a block descriptor's first word, beside col (bits 0-15) and label (16-17).
+constexpr uint32_t kFirst = 1u << 20;  // first block of its tile
+constexpr uint32_t kLast = 1u << 21;   // last block of its tile
+constexpr uint32_t kEnd = 1u << 22;    // no more blocks for this CTA
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 384;  // O accumulator after three 128-column score buffers
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by more
@@ -58,9 +67,11 @@ struct __align__(1024) FwdSmem {
   uint64_t v_full[kStagesV], v_empty[kStagesV];
   uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
   uint64_t o_full, o_empty, drain;
-  // per block: {col | label<<16 | first<<20 | last<<21, stack slot, q_sequence of the tile's first
-  // query, (b*Hq + hq)*Sq + 128*i = output row of the tile's first query}
+  uint64_t info_full[kInfoRing], info_empty[kInfoRing];
+  // per block: {col | label<<16 | flags, stack slot, q_sequence of the tile's first query,
+  // (b*Hq + hq)*Sq + 128*i = Q and output row of the tile's first query}
   uint4 binfo[kInfoRing];
+  uint32_t bkrow[kInfoRing];  // K/V row of the block's first key
   float xmax[2][2][128];    // partial row maxima per [block parity][half][row]
   float xsum[2][128];       // partial row sums per [half][row] at the epilogue
   uint32_t tmem_base;
@@ -105,67 +116,6 @@ __device__ __forceinline__ Tile decode_tile(const FwdParams& p, int32_t T) {
   return t;
 }
 
-// Cursor over this CTA's (tile, block) sequence.  Tiles without blocks are
-// skipped.  Each tile yields exactly row_len blocks: the non-empty MaskInfo
-// positions in order (a malformed row that runs out early is padded with
-// flagged dummy blocks so that every role still sees the same count).  The
-// entry after the one handed out is loaded ahead of use.
-struct Seq {
-  int32_t T;
-  Tile t;
-  int32_t j;    // blocks of the current tile handed out so far
-  int32_t pos;  // MaskInfo position of the entry loaded ahead
-  RawRef ahead;
-  bool valid;
-
-  __device__ __forceinline__ void start_tile(const FwdParams& p) {
-    while (true) {
-      T += gridDim.x;
-      if (T >= p.n_tiles) {
-        valid = false;
-        return;
-      }
-      t = decode_tile(p, T);
-      if (t.n > 0) break;
-    }
-    j = 0;
-    pos = 0;
-    if (p.mi.width > 0) ahead = load_block(p.mi, t.row_base, 0);
-    valid = true;
-  }
-  __device__ __forceinline__ void init(const FwdParams& p) {
-    T = static_cast<int32_t>(blockIdx.x) - static_cast<int32_t>(gridDim.x);
-    start_tile(p);
-  }
-  // Next block; `first`/`last` mark the tile's first and last block.  After
-  // the last block the caller moves on with finish_tile().
-  __device__ __forceinline__ bool next(const FwdParams& p, BlockRef& br, bool& first, bool& last) {
-    if (!valid) return false;
-    bool found = false;
-    while (pos < p.mi.width) {
-      const RawRef cur = ahead;
-      ++pos;
-      if (pos < p.mi.width) ahead = load_block(p.mi, t.row_base, pos);
-      br = check_block(p.mi, cur, p.err);
-      if (br.label != 0) {
-        found = true;
-        break;
-      }
-    }
-    if (!found) {  // malformed row: fewer non-empty entries than row_len
-      if (p.err) atomicOr(p.err, DEV_ERR_BOUNDS);
-      br.label = 2;
-      br.col = 0;
-      br.slot = 0;
-    }
-    first = j == 0;
-    ++j;
-    last = j == t.n;
-    return true;
-  }
-  __device__ __forceinline__ void finish_tile(const FwdParams& p) { start_tile(p); }
-};
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -187,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], 256);
+      mbar_init(&s.p_full[i], 32 * kSoftmaxWarps);
       mbar_init(&s.pv_done[i], 1);
     }
     for (int i = 0; i < kStagesK; ++i) {
@@ -198,8 +148,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_empty[i], 1);
     }
+    for (int i = 0; i < kInfoRing; ++i) {
+      mbar_init(&s.info_full[i], 1);
+      mbar_init(&s.info_empty[i], kInfoReaders);
+    }
     mbar_init(&s.o_full, 1);
-    mbar_init(&s.o_empty, 256);
+    mbar_init(&s.o_empty, 32 * kSoftmaxWarps);
     mbar_init(&s.drain, 1);
     fence_mbar_init();
   }
@@ -214,45 +168,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = __shfl_sync(0xffffffffu, s.tmem_base, 0);
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
 
-  if (warp == 0) {
+  if (warp == 3) {
+    // ------------------------------------------------------------ block walker
+    // Every lane walks the same sequence (same loads, one transaction each);
+    // lane 0 publishes.  Tiles with no block are written here directly.
+    uint32_t n = 0;
+    bool ok = true;
+    auto publish = [&](uint32_t x, uint32_t y, uint32_t z, uint32_t w, uint32_t krow) -> bool {
+      const uint32_t slot = n % kInfoRing;
+      if (n >= static_cast<uint32_t>(kInfoRing) &&
+          !mbar_wait_warp(&s.info_empty[slot], ((n / kInfoRing) - 1) & 1u, wc))
+        return false;
+      if (lane == 0) {
+        s.binfo[slot] = make_uint4(x, y, z, w);
+        s.bkrow[slot] = krow;
+        mbar_arrive(&s.info_full[slot]);
+      }
+      __syncwarp();
+      ++n;
+      return true;
+    };
+    for (int32_t T = blockIdx.x; ok && T < p.n_tiles; T += gridDim.x) {
+      const Tile t = decode_tile(p, T);
+      const int64_t out_row = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128;
+      if (t.n == 0) {
+        // every key masked for the whole query block: O = 0, LSE = -inf
+        uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
+        for (int v = lane; v < 128 * D / 8; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+        for (int r = lane; r < 128; r += 32) p.lse[out_row + r] = -INFINITY;
+        continue;
+      }
+      const uint32_t q0 = static_cast<uint32_t>(p.mi.q_sequence[t.i * 128]);
+      const int64_t kv_base = (static_cast<int64_t>(t.b) * p.Hkv + t.hq / (p.Hq / p.Hkv)) * p.Skv;
+      int32_t j = 0;
+      RawRef ahead = load_block(p.mi, t.row_base, 0);
+      for (int32_t pos = 0; ok && pos < p.mi.width && j < t.n; ++pos) {
+        const RawRef cur = ahead;
+        if (pos + 1 < p.mi.width) ahead = load_block(p.mi, t.row_base, pos + 1);
+        const BlockRef br = check_block(p.mi, cur, lane == 0 ? p.err : nullptr);
+        if (br.label == 0) continue;
+        const uint32_t x = static_cast<uint32_t>(br.col) | (static_cast<uint32_t>(br.label) << 16) |
+                           (j == 0 ? kFirst : 0u) | (j + 1 == t.n ? kLast : 0u);
+        ok = publish(x, static_cast<uint32_t>(br.slot), q0, static_cast<uint32_t>(out_row),
+                     static_cast<uint32_t>(kv_base + static_cast<int64_t>(br.col) * 128));
+        ++j;
+      }
+      // a malformed row with fewer non-empty entries than row_len: flagged
+      // dummy blocks keep every role's count in step
+      for (; ok && j < t.n; ++j) {
+        if (lane == 0 && p.err) atomicOr(p.err, DEV_ERR_BOUNDS);
+        ok = publish((2u << 16) | (j == 0 ? kFirst : 0u) | (j + 1 == t.n ? kLast : 0u), 0u, q0,
+                     static_cast<uint32_t>(out_row), static_cast<uint32_t>(kv_base));
+      }
+    }
+    if (ok) (void)publish(kEnd, 0u, 0u, 0u, 0u);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      uint32_t q_loads = 0, k_loads = 0;
+      uint32_t n = 0, q_loads = 0, k_loads = 0;
       bool ok = true;
-      Seq sq;
-      sq.init(p);
-      BlockRef br;
-      bool first, last;
-      int64_t kv_base = 0;
-      int32_t tile_q0 = 0;
-      uint32_t tile_row = 0;
-      while (ok && sq.next(p, br, first, last)) {
-        if (first) {
-          tile_q0 = p.mi.q_sequence[sq.t.i * 128];
-          tile_row = static_cast<uint32_t>((static_cast<int64_t>(sq.t.b) * p.Hq + sq.t.hq) * p.Sq + sq.t.i * 128);
+      while (ok) {
+        const uint32_t slot = n % kInfoRing;
+        if (!mbar_wait(&s.info_full[slot], (n / kInfoRing) & 1u, wc)) { ok = false; break; }
+        const uint32_t x = s.binfo[slot].x;
+        const uint32_t qrow = s.binfo[slot].w;
+        const uint32_t krow = s.bkrow[slot];
+        const uint32_t ks = k_loads % kStagesK;
+        if (k_loads >= kStagesK && !mbar_wait(&s.k_empty[ks], ((k_loads / kStagesK) - 1) & 1u, wc)) { ok = false; break; }
+        if (x & kEnd) {
+          // no more blocks: complete the stage without data so the MMA warp reads the end mark
+          mbar_arrive(&s.k_full[ks]);
+          break;
+        }
+        if (x & kFirst) {
           const uint32_t qb = q_loads & 1u;
           if (q_loads >= 2 && !mbar_wait(&s.q_empty[qb], ((q_loads >> 1) - 1) & 1u, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.q_full[qb], kTileBytes);
-          const int32_t qrow = static_cast<int32_t>((static_cast<int64_t>(sq.t.b) * p.Hq + sq.t.hq) * p.Sq + sq.t.i * 128);
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(s.q[qb] + c * 16384, &tm_q, &s.q_full[qb], c * 64, qrow, pol_q);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(s.q[qb] + c * 16384, &tm_q, &s.q_full[qb], c * 64, static_cast<int32_t>(qrow), pol_q);
           ++q_loads;
-          kv_base = (static_cast<int64_t>(sq.t.b) * p.Hkv + sq.t.hq / (p.Hq / p.Hkv)) * p.Skv;
         }
-        const uint32_t ks = k_loads % kStagesK;
-        if (k_loads >= kStagesK && !mbar_wait(&s.k_empty[ks], ((k_loads / kStagesK) - 1) & 1u, wc)) { ok = false; break; }
-        s.binfo[k_loads % kInfoRing] =
-            make_uint4(static_cast<uint32_t>(br.col) | (static_cast<uint32_t>(br.label) << 16) | (first ? 1u << 20 : 0u) |
-                           (last ? 1u << 21 : 0u),
-                       static_cast<uint32_t>(br.slot), static_cast<uint32_t>(tile_q0), tile_row);
         mbar_arrive_expect_tx(&s.k_full[ks], kTileBytes);
-        const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
-        for (int c = 0; c < kChunks; ++c) tma_load_2d(s.k[ks] + c * 16384, &tm_k, &s.k_full[ks], c * 64, krow, pol_kv);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(s.k[ks] + c * 16384, &tm_k, &s.k_full[ks], c * 64, static_cast<int32_t>(krow), pol_kv);
         ++k_loads;
-        if (last) sq.finish_tile(p);
+        ++n;
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
@@ -268,22 +272,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_v);
       const uint64_t pol_kv = policy_evict_last();
-      uint32_t v_loads = 0;
+      uint32_t n = 0, v_loads = 0;
       bool ok = true;
-      Seq sq;
-      sq.init(p);
-      BlockRef br;
-      bool first, last;
-      int64_t kv_base = 0;
-      while (ok && sq.next(p, br, first, last)) {
-        if (first) kv_base = (static_cast<int64_t>(sq.t.b) * p.Hkv + sq.t.hq / (p.Hq / p.Hkv)) * p.Skv;
+      while (ok) {
+        const uint32_t slot = n % kInfoRing;
+        if (!mbar_wait(&s.info_full[slot], (n / kInfoRing) & 1u, wc)) { ok = false; break; }
+        const uint32_t x = s.binfo[slot].x;
+        const uint32_t krow = s.bkrow[slot];
+        mbar_arrive(&s.info_empty[slot]);
+        if (x & kEnd) break;
         const uint32_t vs = v_loads % kStagesV;
         if (v_loads >= kStagesV && !mbar_wait(&s.v_empty[vs], ((v_loads / kStagesV) - 1) & 1u, wc)) { ok = false; break; }
         mbar_arrive_expect_tx(&s.v_full[vs], kTileBytes);
-        const int32_t krow = static_cast<int32_t>(kv_base + br.col * 128);
-        for (int c = 0; c < kChunks; ++c) tma_load_2d(s.v[vs] + c * 16384, &tm_v, &s.v_full[vs], c * 64, krow, pol_kv);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(s.v[vs] + c * 16384, &tm_v, &s.v_full[vs], c * 64, static_cast<int32_t>(krow), pol_kv);
         ++v_loads;
-        if (last) sq.finish_tile(p);
+        ++n;
       }
       if (!ok) {
         uint32_t dummy_abort = 0;
@@ -301,18 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t kdesc0 = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
     const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v[0]), 16384, 1024);
     constexpr uint64_t kTileDesc = kTileBytes >> 4;
-    // Total blocks of this CTA (same count every role walks).
-    uint32_t total = 0;
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(decode_tile(p, T).n);
-    uint32_t s_cnt = 0, pv_cnt = 0, q_uses = 0, o_uses = 0;
+    uint32_t s_cnt = 0, pv_cnt = 0, q_uses = 0;
+    uint32_t flags = 0;  // first/last bits of the blocks between P V and S, two per block
     uint64_t cur_q = qdesc0;
-    bool ok = true;
+    bool ok = true, s_end = false;
 
+    // The block descriptor is read after the K stage fills: the K producer
+    // read it (after the walker published it) before filling the stage.
     auto issue_s = [&]() -> bool {
       const uint32_t ks = s_cnt % kStagesK;
       if (!mbar_wait_warp(&s.k_full[ks], (s_cnt / kStagesK) & 1u, wc)) return false;
-      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[s_cnt % kInfoRing].x, 0);
-      if (info & (1u << 20)) {  // first block of a tile: its Q buffer
+      const uint32_t info = s.binfo[s_cnt % kInfoRing].x;
+      if (info & kEnd) {
+        s_end = true;
+        return true;
+      }
+      if (info & kFirst) {  // first block of a tile: its Q buffer
         const uint32_t qb = q_uses & 1u;
         if (!mbar_wait_warp(&s.q_full[qb], (q_uses >> 1) & 1u, wc)) return false;
         cur_q = qdesc0 + qb * kTileDesc;
@@ -327,18 +335,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_elect(&s.s_full[sb]);
       mma_commit_elect(&s.k_empty[ks]);
-      if (info & (1u << 21)) {          // last block of the tile: its Q buffer is free after this S
+      if (info & kLast) {  // last block of the tile: its Q buffer is free after this S
         mma_commit_elect(&s.q_empty[q_uses & 1u]);
         ++q_uses;
       }
+      const uint32_t sh = 2u * (s_cnt & 7u);
+      flags = (flags & ~(3u << sh)) | (((info >> 20) & 3u) << sh);
       ++s_cnt;
       return true;
     };
 
-    while (ok && s_cnt < total && s_cnt < static_cast<uint32_t>(kSBufs)) ok = issue_s();
-    while (ok && pv_cnt < total) {
-      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[pv_cnt % kInfoRing].x, 0);
-      const bool pv_first = (info >> 20) & 1u, pv_last = (info >> 21) & 1u;
+    while (ok && !s_end && s_cnt < static_cast<uint32_t>(kSBufs)) ok = issue_s();
+    uint32_t o_uses = 0;
+    while (ok && pv_cnt < s_cnt) {
+      const uint32_t fl = (flags >> (2u * (pv_cnt & 7u))) & 3u;
+      const bool pv_first = fl & 1u, pv_last = fl & 2u;
       const uint32_t pb = pv_cnt % kSBufs;
       if (!mbar_wait_warp(&s.p_full[pb], (pv_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
       if (pv_first && o_uses > 0 && !mbar_wait_warp(&s.o_empty, (o_uses - 1) & 1u, wc)) { ok = false; break; }
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++pv_cnt;
       // S for the block kSBufs ahead reuses this P buffer: issued after this P V.
-      if (s_cnt < total) ok = issue_s();
+      if (!s_end) ok = issue_s();
     }
     // Every MMA issued so far completes before tensor memory is released.
     mma_commit_elect(&s.drain);
@@ -379,20 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kOCols = D / 2;                               // O columns per half
     const uint32_t ocol0 = kTmemO + static_cast<uint32_t>(half) * kOCols;
     const float scale_log2 = p.scale_log2;
-    uint32_t s_cnt = 0, o_uses = 0;
+    uint32_t n = 0, o_uses = 0;
     bool ok = true;
-    // Tiles without blocks (every key masked for the whole query block)
-    // get O = 0 and LSE = -inf directly.
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) {
-      const Tile t = decode_tile(p, T);
-      if (t.n > 0) continue;
-      const int64_t orow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + half * kOCols);
-      for (int v = 0; v < kOCols / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
-      if (half == 0) p.lse[orow] = -INFINITY;
-    }
-    uint32_t total = 0;
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(decode_tile(p, T).n);
     float m = -INFINITY, l = 0.f;  // l: this half's partial row sum
     int64_t lo = 0, hi = 0;
     uint32_t exec = 0;
@@ -410,38 +409,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* optr = p.o + orow * D + half * kOCols;
       if (!mbar_wait_warp(&s.o_full, o_uses & 1u, wc)) return false;
       tc_fence_after();
-      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
+      // O leaves tensor memory first, so the next tile's P V can start
+      // while this one is scaled and stored.
+      uint32_t ov[kOCols];
 #pragma unroll
-      for (int c = 0; c < kOCols / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tmem + ocol0 + c * 32 + lane_off, ov);
-        tmem_wait_ld();
-        uint4* dst = reinterpret_cast<uint4*>(optr + c * 32);
+      for (int c = 0; c < kOCols / 32; ++c) tmem_ld32(tmem + ocol0 + c * 32 + lane_off, ov + c * 32);
+      tmem_wait_ld();
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 o4;
-          o4.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l);
-          o4.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l);
-          o4.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l);
-          o4.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l);
-          dst[v] = o4;
-        }
-      }
+      for (int c = 0; c < kOCols / 32; ++c) reg_fence32(ov + c * 32);
       tc_fence_before();
       mbar_arrive(&s.o_empty);
       ++o_uses;
+      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(optr);
+#pragma unroll
+      for (int v = 0; v < kOCols / 8; ++v) {
+        uint4 o4;
+        o4.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l);
+        o4.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l);
+        o4.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l);
+        o4.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l);
+        dst[v] = o4;
+      }
       if (half == 0) p.lse[orow] = l_row > 0.f ? (pend_m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
       pending = false;
       return true;
     };
-    while (ok && s_cnt < total) {
-      const uint32_t sb = s_cnt % kSBufs;
-      if (!mbar_wait_warp(&s.s_full[sb], (s_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
-      // block descriptor published by the K producer before this block's K load
-      const uint4 bi = s.binfo[s_cnt % kInfoRing];
+    while (ok) {
+      // block descriptor from the walker (published long before its scores)
+      const uint32_t slot = n % kInfoRing;
+      if (!mbar_wait_warp(&s.info_full[slot], (n / kInfoRing) & 1u, wc)) { ok = false; break; }
+      const uint4 bi = s.binfo[slot];
+      if (bi.x & kEnd) break;
+      const uint32_t sb = n % kSBufs;
+      if (!mbar_wait_warp(&s.s_full[sb], (n / kSBufs) & 1u, wc)) { ok = false; break; }
+      // Released only now: the scores being ready means the K producer and
+      // the MMA warp have read this descriptor too.
+      if (lane == 0) mbar_arrive(&s.info_empty[slot]);
       const int32_t col = static_cast<int32_t>(bi.x & 0xFFFFu);
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
-      const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
+      const bool first = bi.x & kFirst, last = bi.x & kLast;
       if (first) {
         m = -INFINITY;
         l = 0.f;
@@ -450,13 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.mi.kind != BSA_MASK_DENSE)
           key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(static_cast<int32_t>(bi.z)) + r,
                        lo, hi);
-      }
-      tc_fence_after();
-      uint32_t xu[64];
-      {
-        const uint32_t sa = tmem + sb * 128 + col0 + lane_off;
-        tmem_ld32(sa + 0, xu + 0);
-        tmem_ld32(sa + 32, xu + 32);
       }
       uint32_t mbits[2] = {~0u, ~0u};  // visibility of this half's 64 columns (label 1 only)
       if (label == 1) {
@@ -492,7 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // no branch joins while the loaded registers are in flight
+      tc_fence_after();
+      uint32_t xu[64];
+      {
+        const uint32_t sa = tmem + sb * 128 + col0 + lane_off;
+        tmem_ld32(sa + 0, xu + 0);
+        tmem_ld32(sa + 32, xu + 32);
+      }
       tmem_wait_ld();
+      reg_fence32(xu);
+      reg_fence32(xu + 32);
       if (label == 1) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
@@ -510,9 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float pm = fmax3(fmaxf(m0, m1), m2, m3);
       // exchange with the other half of the row (double-buffered by block parity)
-      s.xmax[s_cnt & 1u][half][r] = pm;
+      s.xmax[n & 1u][half][r] = pm;
       named_bar_sync(bar_id, 64);
-      const float mx = fmaxf(pm, s.xmax[s_cnt & 1u][half ^ 1][r]);
+      const float mx = fmaxf(pm, s.xmax[n & 1u][half ^ 1][r]);
       const float m_blk = mx * scale_log2;
       const float m_cand = fmaxf(m, m_blk);
       const bool switch_ref = m_cand > m + kRescaleThreshold;
@@ -549,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O holds earlier blocks' sum only after the first block; rescale this
       // half's O columns (after the previous P V has landed) when the max moved.
       if (warp_switch && exec > 0) {
-        const uint32_t prev = s_cnt - 1;
+        const uint32_t prev = n - 1;
         if (!mbar_wait_warp(&s.pv_done[prev % kSBufs], (prev / kSBufs) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
         const uint64_t al2 = f2_pack(alpha, alpha);
@@ -559,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t oa = tmem + ocol0 + c * 32 + lane_off;
           tmem_ld32(oa, ov);
           tmem_wait_ld();
+          reg_fence32(ov);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const uint64_t o2 = f2_mul(f2_pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), al2);
@@ -573,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.p_full[sb]);
-      ++s_cnt;
+      ++n;
       ++exec;
       if (first && pending && !epilogue()) { ok = false; break; }
       if (last) {

@@ -75,13 +75,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` (it resumes as
+// soon as the phase completes), so that a waiting warp does not take issue
+// slots from the warps sharing its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0u;
+}
+
 // Slow path of mbar_wait, kept out of line so the callers' loops stay small.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, uint32_t* err, volatile uint32_t* abort,
                                             uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 63u) {
+    if (mbar_try_wait_suspend(a, parity, 20000u)) return true;
+    if ((it & 3u) == 3u) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         if (err) atomicOr(err, DEV_ERR_TIMEOUT);
@@ -305,6 +320,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
         "=r"(r[15])
       : "r"(taddr)
       : "memory");
+}
+
+// tcgen05.ld returns before its data lands in the registers; the data is
+// valid after tcgen05.wait::ld.  These empty statements, placed after the
+// wait, make the loaded registers depend on it, so that the compiler cannot
+// schedule a use of them before the wait.
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+__device__ __forceinline__ void reg_fence16(uint32_t* r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i < N; i += 16) reg_fence16(r + i);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
