@@ -21,8 +21,11 @@
 //   warp 2      TMA producer of V blocks (2 stages)
 //   warps 4-11  softmax in two warpgroups, one (row, half of the columns)
 //               per thread: mask, row max (halves exchanged through shared
-//               memory), exp2, row sum, P to TMEM, lazy O rescale in TMEM,
-//               epilogue
+//               memory), exp2, row sum, P to TMEM, lazy O rescale in TMEM;
+//               at a tile's end the row statistics go to shared memory and
+//               the softmax moves straight on to the next tile
+//   warps 12-15 epilogue: O / l from TMEM to bf16 in HBM and the
+//               logsumexp, one row per thread, while the next tile runs
 // Each CTA walks one fixed sequence of (tile, block) pairs; every role
 // walks it the same way, so the pipelines stay in step without sharing
 // state.  Work tiles are (batch, query head, query block), longest rows
@@ -42,8 +45,14 @@ constexpr int kStagesK = 2;
 constexpr int kStagesV = 2;
 constexpr int kSBufs = 3;         // score buffers in TMEM
 constexpr int kInfoRing = 32;     // block descriptors published by the walker warp
-constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = 128 + 32 * kSoftmaxWarps;  // 4 role warps + the softmax warps
+// The softmax is split over kParts warpgroups, each taking kCols of the 128
+// score columns of every row (and D / kParts of the O columns).
+constexpr int kParts = 2;
+constexpr int kCols = 128 / kParts;
+constexpr int kSoftmaxWarps = 4 * kParts;
+// 4 role warps + the softmax warps + one epilogue warpgroup
+constexpr int kThreads = 128 + 32 * kSoftmaxWarps + 128;
+constexpr int kEpiWarp0 = 4 + kSoftmaxWarps;  // first warp of the epilogue warpgroup
 // Readers that release a block descriptor: the V producer and every softmax
 // warp.  A softmax warp releases it once the block's scores are ready, by
 // when the K producer and the MMA warp have read it too.
@@ -72,8 +81,13 @@ struct __align__(1024) FwdSmem {
   // (b*Hq + hq)*Sq + 128*i = Q and output row of the tile's first query}
   uint4 binfo[kInfoRing];
   uint32_t bkrow[kInfoRing];  // K/V row of the block's first key
-  float xmax[2][2][128];    // partial row maxima per [block parity][half][row]
-  float xsum[2][128];       // partial row sums per [half][row] at the epilogue
+  float xmax[2][kParts][128];  // partial row maxima per [block parity][part][row]
+  // a finished tile's row statistics for the epilogue warpgroup, per [tile
+  // parity]: the row maximum (log2 units) and each part's partial row sum
+  float tmax[2][128];
+  float tsum[2][kParts][128];
+  uint32_t trow[2];              // output row of the tile's first query
+  uint64_t stats_full[2], stats_empty[2];
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -153,7 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.info_empty[i], kInfoReaders);
     }
     mbar_init(&s.o_full, 1);
-    mbar_init(&s.o_empty, 32 * kSoftmaxWarps);
+    mbar_init(&s.o_empty, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.stats_full[i], 32 * kSoftmaxWarps);
+      mbar_init(&s.stats_empty[i], 128);
+    }
     mbar_init(&s.drain, 1);
     fence_mbar_init();
   }
@@ -376,63 +394,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t dummy_abort = 0;
     WaitCtl dw{p.err, &dummy_abort, p.wait_ns};
     (void)mbar_wait(&s.drain, 0, dw);
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue warpgroup
+    // One query row per thread: waits for a tile's statistics and its final
+    // O, reads O out of tensor memory (then releases it for the next tile's
+    // P V) and writes O / l in bf16 and the logsumexp.
+    const int quarter = warp - kEpiWarp0;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t obase = tmem + kTmemO + lane_off;
+    bool ok = true;
+    for (uint32_t t = 0; ok; ++t) {
+      const uint32_t tp = t & 1u;
+      if (!mbar_wait_warp(&s.stats_full[tp], (t >> 1) & 1u, wc)) { ok = false; break; }
+      const uint32_t row0 = s.trow[tp];
+      if (row0 == 0xFFFFFFFFu) break;  // end mark from the softmax warps
+      const float mrow = s.tmax[tp][r];
+      float l_row = 0.f;
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) l_row += s.tsum[tp][q][r];
+      mbar_arrive(&s.stats_empty[tp]);
+      if (!mbar_wait_warp(&s.o_full, t & 1u, wc)) { ok = false; break; }
+      tc_fence_after();
+      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
+      const int64_t orow = static_cast<int64_t>(row0) + r;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
+      // chunks of 32 columns, the next one in flight while this one is
+      // scaled and stored (straight-line code up to each wait)
+      uint32_t va[32], vb[32];
+      auto emit = [&](const uint32_t* v, int c) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint4 o4;
+          o4.x = pack_bf16x2(__uint_as_float(v[8 * e + 0]) * inv_l, __uint_as_float(v[8 * e + 1]) * inv_l);
+          o4.y = pack_bf16x2(__uint_as_float(v[8 * e + 2]) * inv_l, __uint_as_float(v[8 * e + 3]) * inv_l);
+          o4.z = pack_bf16x2(__uint_as_float(v[8 * e + 4]) * inv_l, __uint_as_float(v[8 * e + 5]) * inv_l);
+          o4.w = pack_bf16x2(__uint_as_float(v[8 * e + 6]) * inv_l, __uint_as_float(v[8 * e + 7]) * inv_l);
+          dst[c * 4 + e] = o4;
+        }
+      };
+      tmem_ld32(obase, va);
+      tmem_wait_ld();
+      reg_fence32(va);
+#pragma unroll
+      for (int c = 0; c < D / 32; c += 2) {
+        if (c + 1 < D / 32) tmem_ld32(obase + (c + 1) * 32, vb);
+        emit(va, c);
+        if (c + 1 < D / 32) {
+          tmem_wait_ld();
+          reg_fence32(vb);
+          if (c + 2 < D / 32) tmem_ld32(obase + (c + 2) * 32, va);
+          emit(vb, c + 1);
+          if (c + 2 < D / 32) {
+            tmem_wait_ld();
+            reg_fence32(va);
+          }
+        }
+      }
+      // (every load of this tile's O has completed by the last wait)
+      tc_fence_before();
+      mbar_arrive(&s.o_empty);
+      p.lse[orow] = l_row > 0.f ? (mrow + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+    }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax (two warpgroups)
-    // Warpgroup `half` takes score columns [64*half, 64*half+64) of every
-    // row; warps w and w+4 share TMEM lanes (rows) and exchange their
-    // partial row maxima through shared memory under a 64-thread barrier.
-    const int half = (warp - 4) >> 2;
+    // ------------------------------------------------------------ softmax (kParts warpgroups)
+    // Warpgroup `part` takes score columns [kCols*part, kCols*part + kCols)
+    // of every row; the warps with the same lanes (rows) in the kParts
+    // warpgroups exchange their partial row maxima through shared memory.
+    constexpr int kOCols = D / kParts;  // O columns per part
+    const int part = (warp - 4) >> 2;
     const int quarter = (warp - 4) & 3;
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
     const uint32_t bar_id = 1u + static_cast<uint32_t>(quarter);
+    constexpr uint32_t kBarThreads = 32 * kParts;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t col0 = static_cast<uint32_t>(half) * 64;     // first score column of this half
-    constexpr int kOCols = D / 2;                               // O columns per half
-    const uint32_t ocol0 = kTmemO + static_cast<uint32_t>(half) * kOCols;
+    const uint32_t col0 = static_cast<uint32_t>(part) * kCols;  // first score column of this part
+    const uint32_t ocol0 = kTmemO + static_cast<uint32_t>(part) * kOCols;
     const float scale_log2 = p.scale_log2;
-    uint32_t n = 0, o_uses = 0;
+    uint32_t n = 0;
     bool ok = true;
-    float m = -INFINITY, l = 0.f;  // l: this half's partial row sum
+    float m = -INFINITY, l = 0.f;  // l: this part's partial row sum
     int64_t lo = 0, hi = 0;
     uint32_t exec = 0;
-    // A finished tile's epilogue waits until the next tile's first block has
-    // been handed to the tensor cores, so the softmax never idles on the
-    // tile's last P V.
-    bool pending = false;
-    float pend_m = 0.f, pend_l = 0.f;
-    uint32_t pend_row = 0;
-    auto epilogue = [&]() -> bool {
-      s.xsum[half][r] = pend_l;
-      named_bar_sync(bar_id, 64);
-      const float l_row = pend_l + s.xsum[half ^ 1][r];
-      const int64_t orow = static_cast<int64_t>(pend_row) + r;
-      __nv_bfloat16* optr = p.o + orow * D + half * kOCols;
-      if (!mbar_wait_warp(&s.o_full, o_uses & 1u, wc)) return false;
-      tc_fence_after();
-      // O leaves tensor memory first, so the next tile's P V can start
-      // while this one is scaled and stored.
-      uint32_t ov[kOCols];
-#pragma unroll
-      for (int c = 0; c < kOCols / 32; ++c) tmem_ld32(tmem + ocol0 + c * 32 + lane_off, ov + c * 32);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < kOCols / 32; ++c) reg_fence32(ov + c * 32);
-      tc_fence_before();
-      mbar_arrive(&s.o_empty);
-      ++o_uses;
-      const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(optr);
-#pragma unroll
-      for (int v = 0; v < kOCols / 8; ++v) {
-        uint4 o4;
-        o4.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l);
-        o4.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l);
-        o4.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l);
-        o4.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l);
-        dst[v] = o4;
-      }
-      if (half == 0) p.lse[orow] = l_row > 0.f ? (pend_m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
-      pending = false;
+    uint32_t tiles = 0;
+    // Hands a finished tile's row statistics to the epilogue warpgroup.
+    auto finish_tile = [&](uint32_t row) -> bool {
+      const uint32_t tp = tiles & 1u;
+      if (tiles >= 2 && !mbar_wait_warp(&s.stats_empty[tp], ((tiles >> 1) - 1) & 1u, wc)) return false;
+      if (part == 0) s.tmax[tp][r] = (m == -INFINITY) ? 0.f : m;
+      s.tsum[tp][part][r] = l;
+      if (r == 0 && part == 0) s.trow[tp] = row;
+      mbar_arrive(&s.stats_full[tp]);
+      ++tiles;
       return true;
     };
     while (ok) {
@@ -458,75 +511,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(static_cast<int32_t>(bi.z)) + r,
                        lo, hi);
       }
-      uint32_t mbits[2] = {~0u, ~0u};  // visibility of this half's 64 columns (label 1 only)
+      uint64_t mbits = ~0ull;  // visibility of this part's columns (label 1 only)
       if (label == 1) {
         if (p.mi.kind == BSA_MASK_DENSE) {
           const uint4* mrow = reinterpret_cast<const uint4*>(
               p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
+          mbits = 0;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
+          for (int v = 0; v < kCols / 16; ++v) {
             const uint4 mw = __ldg(mrow + v);
             const uint32_t wv[4] = {mw.x, mw.y, mw.z, mw.w};
-            uint32_t bits = 0;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) bits |= (((wv[e >> 2] >> ((e & 3) * 8)) & 0xFFu) != 0u ? 1u : 0u) << e;
-            if (v & 1) mbits[v >> 1] |= bits << 16;
-            else mbits[v >> 1] = bits;
+            for (int e = 0; e < 16; ++e)
+              mbits |= static_cast<uint64_t>(((wv[e >> 2] >> ((e & 3) * 8)) & 0xFFu) != 0u ? 1u : 0u) << (v * 16 + e);
           }
         } else {
-          // visible columns of this row form [a, b] inside this half
+          // visible columns of this row form [a, b] inside this part
           const int64_t k0 = static_cast<int64_t>(col) * 128 + col0;
           const int64_t a64 = lo - k0, b64 = hi - k0;
-          const int32_t a = a64 < 0 ? 0 : (a64 > 64 ? 64 : static_cast<int32_t>(a64));
-          const int32_t b = b64 > 63 ? 63 : (b64 < -1 ? -1 : static_cast<int32_t>(b64));
-#pragma unroll
-          for (int w32 = 0; w32 < 2; ++w32) {
-            const int32_t lo_c = a - w32 * 32, hi_c = b - w32 * 32;  // inclusive range in this word
-            uint32_t bits = 0;
-            if (hi_c >= 0 && lo_c <= 31 && hi_c >= lo_c) {
-              const int32_t l0 = lo_c < 0 ? 0 : lo_c, h0 = hi_c > 31 ? 31 : hi_c;
-              const uint32_t upto = h0 >= 31 ? 0xFFFFFFFFu : ((1u << (h0 + 1)) - 1u);
-              bits = upto & ~((1u << l0) - 1u);
-            }
-            mbits[w32] = bits;
+          const int32_t a = a64 < 0 ? 0 : (a64 > kCols ? kCols : static_cast<int32_t>(a64));
+          const int32_t b = b64 > kCols - 1 ? kCols - 1 : (b64 < -1 ? -1 : static_cast<int32_t>(b64));
+          if (b < a) {
+            mbits = 0;
+          } else {
+            const uint64_t upto = b >= 63 ? ~0ull : ((1ull << (b + 1)) - 1ull);
+            mbits = upto & ~((1ull << a) - 1ull);
           }
         }
       }
       // no branch joins while the loaded registers are in flight
       tc_fence_after();
-      uint32_t xu[64];
-      {
-        const uint32_t sa = tmem + sb * 128 + col0 + lane_off;
-        tmem_ld32(sa + 0, xu + 0);
-        tmem_ld32(sa + 32, xu + 32);
-      }
+      uint32_t xu[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + sb * 128 + col0 + c + lane_off, xu + c);
       tmem_wait_ld();
-      reg_fence32(xu);
-      reg_fence32(xu + 32);
+      reg_fence<kCols>(xu);
       if (label == 1) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (!((mbits[c >> 5] >> (c & 31)) & 1u)) xu[c] = 0xFF800000u;  // -inf
+        for (int c = 0; c < kCols; ++c)
+          if (!((mbits >> c) & 1ull)) xu[c] = 0xFF800000u;  // -inf
       }
-      // partial row max over this half: four chains of three-input maxima
+      // partial row max over this part: four chains of three-input maxima
       float m0 = __uint_as_float(xu[0]), m1 = __uint_as_float(xu[1]);
       float m2 = __uint_as_float(xu[2]), m3 = __uint_as_float(xu[3]);
 #pragma unroll
-      for (int c = 4; c < 64; c += 8) {
+      for (int c = 4; c < kCols; c += 8) {
         m0 = fmax3(m0, __uint_as_float(xu[c + 0]), __uint_as_float(xu[c + 1]));
         m1 = fmax3(m1, __uint_as_float(xu[c + 2]), __uint_as_float(xu[c + 3]));
         m2 = fmax3(m2, __uint_as_float(xu[c + 4]), __uint_as_float(xu[c + 5]));
         m3 = fmax3(m3, __uint_as_float(xu[c + 6]), __uint_as_float(xu[c + 7]));
       }
       const float pm = fmax3(fmaxf(m0, m1), m2, m3);
-      // exchange with the other half of the row (double-buffered by block parity)
-      s.xmax[n & 1u][half][r] = pm;
-      named_bar_sync(bar_id, 64);
-      const float mx = fmaxf(pm, s.xmax[n & 1u][half ^ 1][r]);
+      // exchange with the other parts of the row (double-buffered by block parity)
+      s.xmax[n & 1u][part][r] = pm;
+      named_bar_sync(bar_id, kBarThreads);
+      float mx = s.xmax[n & 1u][0][r];
+#pragma unroll
+      for (int q = 1; q < kParts; ++q) mx = fmaxf(mx, s.xmax[n & 1u][q][r]);
       const float m_blk = mx * scale_log2;
       const float m_cand = fmaxf(m, m_blk);
       const bool switch_ref = m_cand > m + kRescaleThreshold;
-      const bool warp_switch = __any_sync(0xffffffffu, switch_ref);  // same rows, same values in both halves
+      const bool warp_switch = __any_sync(0xffffffffu, switch_ref);  // same rows, same values in every part
       float alpha = 1.f;
       if (warp_switch) {
         alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_cand);
@@ -538,9 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t acc[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) acc[a] = f2_pack(0.f, 0.f);
-      uint32_t pk[32];
+      uint32_t pk[kCols / 2];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < kCols / 2; ++c) {
         const uint64_t e2 = f2_fma(f2_pack(__uint_as_float(xu[2 * c]), __uint_as_float(xu[2 * c + 1])), sc2, nm2);
         float e0, e1;
         f2_unpack(e2, e0, e1);
@@ -553,32 +598,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       f2_unpack(acc01, rs0, rs1);
       l = l * alpha + (rs0 + rs1);
       // P (bf16 pairs) over the first 64 columns of the score buffer: this
-      // half's 64 probabilities go to words [32*half, 32*half+32); both
-      // halves finished reading their scores before the exchange barrier.
-      tmem_st32(tmem + sb * 128 + static_cast<uint32_t>(half) * 32 + lane_off, pk);
+      // part's probabilities go to words [part*kCols/2, (part+1)*kCols/2);
+      // every part finished reading its scores before the exchange barrier.
+#pragma unroll
+      for (int c = 0; c < kCols / 2; c += 16)
+        tmem_st16(tmem + sb * 128 + static_cast<uint32_t>(part) * (kCols / 2) + c + lane_off, pk + c);
       // O holds earlier blocks' sum only after the first block; rescale this
-      // half's O columns (after the previous P V has landed) when the max moved.
+      // part's O columns (after the previous P V has landed) when the max moved.
       if (warp_switch && exec > 0) {
         const uint32_t prev = n - 1;
         if (!mbar_wait_warp(&s.pv_done[prev % kSBufs], (prev / kSBufs) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
         const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
-        for (int c = 0; c < kOCols / 32; ++c) {
-          uint32_t ov[32];
-          const uint32_t oa = tmem + ocol0 + c * 32 + lane_off;
-          tmem_ld32(oa, ov);
+        for (int c = 0; c < kOCols; c += 16) {
+          uint32_t ov[16];
+          const uint32_t oa = tmem + ocol0 + c + lane_off;
+          tmem_ld16(oa, ov);
           tmem_wait_ld();
-          reg_fence32(ov);
+          reg_fence16(ov);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 16; e += 2) {
             const uint64_t o2 = f2_mul(f2_pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), al2);
             float a0, a1;
             f2_unpack(o2, a0, a1);
             ov[e] = __float_as_uint(a0);
             ov[e + 1] = __float_as_uint(a1);
           }
-          tmem_st32(oa, ov);
+          tmem_st16(oa, ov);
         }
       }
       tmem_wait_st();
@@ -586,15 +633,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&s.p_full[sb]);
       ++n;
       ++exec;
-      if (first && pending && !epilogue()) { ok = false; break; }
-      if (last) {
-        pending = true;
-        pend_m = (m == -INFINITY) ? 0.f : m;
-        pend_l = l;
-        pend_row = bi.w;
+      if (last && !finish_tile(bi.w)) { ok = false; break; }
+    }
+    // end mark for the epilogue warpgroup
+    if (ok) {
+      const uint32_t tp = tiles & 1u;
+      if (tiles < 2 || mbar_wait_warp(&s.stats_empty[tp], ((tiles >> 1) - 1) & 1u, wc)) {
+        if (r == 0 && part == 0) s.trow[tp] = 0xFFFFFFFFu;
+        mbar_arrive(&s.stats_full[tp]);
       }
     }
-    if (ok && pending) ok = epilogue();
   }
 
   tc_fence_before();
