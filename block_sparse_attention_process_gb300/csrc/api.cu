@@ -5,6 +5,8 @@
 #include <mutex>
 #include <string>
 
+#include <cstdlib>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -41,6 +43,14 @@ uint32_t* device_error_word() {
 }
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns; }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("BSA_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
 
 int num_sms() {
   static int sms[64] = {0};

@@ -310,6 +310,9 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
   // broadcast from lane 0 so the compiler keeps it in a uniform register
   const uint32_t tmem = __shfl_sync(0xffffffffu, s.tmem_base, 0);
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
+  // set-up done: the next kernel may launch; this one waits for the previous
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------ Q/dO/LSE/Dsum (per tile) and K (per block); block ring
@@ -745,6 +748,9 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
   // broadcast from lane 0 so the compiler keeps it in a uniform register
   const uint32_t tmem = __shfl_sync(0xffffffffu, s.tmem_base, 0);
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
+  // set-up done: the next kernel may launch; this one waits for the previous
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------ K/V (per tile), Q/dO/LSE/Dsum (per item); item ring
@@ -1072,8 +1078,8 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  dkv_kernel<D><<<grid, DkvShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(dkv_kernel<D>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dkv launch");
   return BSA_OK;
 }
@@ -1094,8 +1100,8 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  dq_kernel<D><<<grid, DqShape<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(dq_kernel<D>, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dq launch");
   return BSA_OK;
 }

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) rowsum_kernel(const uint4* __restrict__ d
                                                      float* __restrict__ dsum, int64_t n_rows) {
   constexpr int kLanesPerRow = D / 8;  // 16 bytes (8 bf16) per lane
   constexpr int kRowsPerCta = 256 / kLanesPerRow;
+  griddep_launch_dependents();
+  griddep_wait();  // O comes from the forward kernel
   const int sub = threadIdx.x % kLanesPerRow;
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + threadIdx.x / kLanesPerRow; row < n_rows;
        row += static_cast<int64_t>(gridDim.x) * kRowsPerCta) {
@@ -45,13 +47,11 @@ bsa_status rowsum_launch(const bsa_bwd_args* a, cudaStream_t stream) {
   const int rows_per_cta = 256 / (a->D / 8);
   const int64_t need = (n_rows + rows_per_cta - 1) / rows_per_cta;
   const int grid = static_cast<int>(std::min<int64_t>(need, static_cast<int64_t>(num_sms()) * 16));
-  if (a->D == 128)
-    rowsum_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(a->do_), static_cast<const uint4*>(a->o),
-                                                 a->dsum, n_rows);
-  else
-    rowsum_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(a->do_), static_cast<const uint4*>(a->o),
-                                                a->dsum, n_rows);
-  cudaError_t e = cudaGetLastError();
+  const uint4* dout = static_cast<const uint4*>(a->do_);
+  const uint4* out = static_cast<const uint4*>(a->o);
+  cudaError_t e = a->D == 128 ? launch_kernel(rowsum_kernel<128>, dim3(grid), dim3(256), 0, stream, dout, out, a->dsum, n_rows)
+                              : launch_kernel(rowsum_kernel<64>, dim3(grid), dim3(256), 0, stream, dout, out, a->dsum, n_rows);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "rowsum launch");
   return BSA_OK;
 }

@@ -185,6 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // broadcast from lane 0 so the compiler keeps it in a uniform register
   const uint32_t tmem = __shfl_sync(0xffffffffu, s.tmem_base, 0);
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
+  // set-up done: the next kernel may launch; this one waits for the previous
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 3) {
     // ------------------------------------------------------------ block walker
@@ -686,8 +689,8 @@ bsa_status launch_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, float sc
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  fwd_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(fwd_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return BSA_OK;
 }

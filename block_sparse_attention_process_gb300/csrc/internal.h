@@ -49,4 +49,26 @@ bsa_status debug_wait_timeout_launch(cudaStream_t stream);
 
 int num_sms();
 
+// Programmatic dependent launch: a kernel launched this way may start (its
+// set-up: barriers, tensor memory, descriptor prefetch) while the previous
+// kernel in the stream finishes; it waits (griddepcontrol.wait) before it
+// touches global memory.  Off when the environment sets BSA_PDL=0.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 }  // namespace bsa
