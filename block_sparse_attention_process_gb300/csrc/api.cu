@@ -251,6 +251,8 @@ bsa_status bsa_mask_info_destroy(bsa_mask_info* info) {
                   info->q_sequence, info->row_len,   info->row_order};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  for (auto& sc : info->schedules)
+    if (sc.dev) cudaFree(sc.dev);
   delete info;
   return BSA_OK;
 }

@@ -100,35 +100,11 @@ struct FwdParams {
   float* lse;
   MaskInfoDev mi;
   int32_t n_tiles;
+  const int4* sched;     // this launch's tile lists, sched_stride entries per CTA
+  int32_t sched_stride;
   uint32_t* err;
   uint64_t wait_ns;
 };
-
-struct Tile {
-  int32_t b, hq, i, hm, n;
-  int64_t row_base;
-};
-
-__device__ __forceinline__ Tile decode_tile(const FwdParams& p, int32_t T) {
-  Tile t;
-  if (p.mi.heads == 1) {
-    const int32_t bh = T % (p.B * p.Hq);
-    const int32_t rank = T / (p.B * p.Hq);
-    t.i = p.mi.row_order[rank];
-    t.b = bh / p.Hq;
-    t.hq = bh % p.Hq;
-    t.hm = 0;
-  } else {
-    t.b = T % p.B;
-    const int32_t row = p.mi.row_order[T / p.B];
-    t.hm = row / p.mi.rows;
-    t.i = row % p.mi.rows;
-    t.hq = t.hm;
-  }
-  t.n = p.mi.row_len[t.hm * p.mi.rows + t.i];
-  t.row_base = (static_cast<int64_t>(t.hm) * p.mi.rows + t.i) * p.mi.width;
-  return t;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -185,9 +161,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // broadcast from lane 0 so the compiler keeps it in a uniform register
   const uint32_t tmem = __shfl_sync(0xffffffffu, s.tmem_base, 0);
   const WaitCtl wc{p.err, &s.abort_flag, p.wait_ns};
-  // set-up done: the next kernel may launch; this one waits for the previous
+  // Set-up done: the next kernel may launch.  This one waits for the
+  // previous kernel (griddep_wait) only in the roles that touch Q/K/V or
+  // write O/LSE; MaskInfo is complete when its compile returns, so the
+  // walker starts right away.
   griddep_launch_dependents();
-  griddep_wait();
 
   if (warp == 3) {
     // ------------------------------------------------------------ block walker
@@ -209,36 +187,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n;
       return true;
     };
-    for (int32_t T = blockIdx.x; ok && T < p.n_tiles; T += gridDim.x) {
-      const Tile t = decode_tile(p, T);
-      const int64_t out_row = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128;
-      if (t.n == 0) {
+    // this CTA's tiles: {MaskInfo row, blocks, b * Hq + hq, query block}, next one loaded ahead
+    const int4* mine = p.sched + static_cast<int64_t>(blockIdx.x) * p.sched_stride;
+    int4 ahead_tile = mine[0];
+    for (int32_t k = 0; ok && k < p.sched_stride; ++k) {
+      const int4 te = ahead_tile;
+      if (te.y < 0) break;
+      if (k + 1 < p.sched_stride) ahead_tile = mine[k + 1];
+      const int32_t t_n = te.y, t_i = te.w;
+      const int32_t t_b = te.z / p.Hq, t_hq = te.z % p.Hq;
+      const int64_t t_row_base = static_cast<int64_t>(te.x) * p.mi.width;
+      const int64_t out_row = static_cast<int64_t>(te.z) * p.Sq + static_cast<int64_t>(t_i) * 128;
+      if (t_n == 0) {
         // every key masked for the whole query block: O = 0, LSE = -inf
+        griddep_wait();
         uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
         for (int v = lane; v < 128 * D / 8; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
         for (int r = lane; r < 128; r += 32) p.lse[out_row + r] = -INFINITY;
         continue;
       }
-      const uint32_t q0 = static_cast<uint32_t>(p.mi.q_sequence[t.i * 128]);
-      const int64_t kv_base = (static_cast<int64_t>(t.b) * p.Hkv + t.hq / (p.Hq / p.Hkv)) * p.Skv;
+      const uint32_t q0 = static_cast<uint32_t>(p.mi.q_sequence[t_i * 128]);
+      const int64_t kv_base = (static_cast<int64_t>(t_b) * p.Hkv + t_hq / (p.Hq / p.Hkv)) * p.Skv;
       int32_t j = 0;
-      RawRef ahead = load_block(p.mi, t.row_base, 0);
-      for (int32_t pos = 0; ok && pos < p.mi.width && j < t.n; ++pos) {
+      RawRef ahead = load_block(p.mi, t_row_base, 0);
+      for (int32_t pos = 0; ok && pos < p.mi.width && j < t_n; ++pos) {
         const RawRef cur = ahead;
-        if (pos + 1 < p.mi.width) ahead = load_block(p.mi, t.row_base, pos + 1);
+        if (pos + 1 < p.mi.width) ahead = load_block(p.mi, t_row_base, pos + 1);
         const BlockRef br = check_block(p.mi, cur, lane == 0 ? p.err : nullptr);
         if (br.label == 0) continue;
         const uint32_t x = static_cast<uint32_t>(br.col) | (static_cast<uint32_t>(br.label) << 16) |
-                           (j == 0 ? kFirst : 0u) | (j + 1 == t.n ? kLast : 0u);
+                           (j == 0 ? kFirst : 0u) | (j + 1 == t_n ? kLast : 0u);
         ok = publish(x, static_cast<uint32_t>(br.slot), q0, static_cast<uint32_t>(out_row),
                      static_cast<uint32_t>(kv_base + static_cast<int64_t>(br.col) * 128));
         ++j;
       }
       // a malformed row with fewer non-empty entries than row_len: flagged
       // dummy blocks keep every role's count in step
-      for (; ok && j < t.n; ++j) {
+      for (; ok && j < t_n; ++j) {
         if (lane == 0 && p.err) atomicOr(p.err, DEV_ERR_BOUNDS);
-        ok = publish((2u << 16) | (j == 0 ? kFirst : 0u) | (j + 1 == t.n ? kLast : 0u), 0u, q0,
+        ok = publish((2u << 16) | (j == 0 ? kFirst : 0u) | (j + 1 == t_n ? kLast : 0u), 0u, q0,
                      static_cast<uint32_t>(out_row), static_cast<uint32_t>(kv_base));
       }
     }
@@ -248,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
+      griddep_wait();
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
       uint32_t n = 0, q_loads = 0, k_loads = 0;
@@ -292,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ V producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_v);
+      griddep_wait();
       const uint64_t pol_kv = policy_evict_last();
       uint32_t n = 0, v_loads = 0;
       bool ok = true;
@@ -406,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t obase = tmem + kTmemO + lane_off;
+    griddep_wait();
     bool ok = true;
     for (uint32_t t = 0; ok; ++t) {
       const uint32_t tp = t & 1u;
@@ -689,6 +679,9 @@ bsa_status launch_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, float sc
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
+  const int64_t units = info->heads == 1 ? static_cast<int64_t>(a->B) * a->Hq : a->B;
+  bsa_status st = tile_schedule(info, units, a->Hq, grid, &p.sched, &p.sched_stride);
+  if (st != BSA_OK) return st;
   cudaError_t e = launch_kernel(fwd_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");

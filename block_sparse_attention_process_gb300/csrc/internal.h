@@ -2,7 +2,9 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <mutex>
 #include <string>
+#include <vector>
 
 #include "bsa.h"
 
@@ -23,6 +25,16 @@ struct bsa_mask_info {
   int32_t* q_sequence = nullptr;     // [q_len]
   int32_t* row_len = nullptr;        // [heads, rows] non-empty blocks per row (internal)
   int32_t* row_order = nullptr;      // [heads * rows] rows sorted by decreasing row_len (internal)
+  // host copies of row_len / row_order, for the launch-time tile schedules
+  std::vector<int32_t> row_len_h, row_order_h;
+  // tile schedules built so far (device memory, freed with the handle)
+  struct Schedule {
+    int64_t units = 0;
+    int32_t hq = 0, grid = 0, device = -1, stride = 0;
+    int4* dev = nullptr;
+  };
+  mutable std::vector<Schedule> schedules;
+  mutable std::mutex sched_mu;
 };
 
 namespace bsa {
@@ -48,6 +60,17 @@ bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
 bsa_status debug_wait_timeout_launch(cudaStream_t stream);
 
 int num_sms();
+
+// Work tiles of a launch: every MaskInfo row (row_order order, longest
+// first) times `units` (B * Hq for a shared mask, B for per-head masks),
+// handed to `grid` persistent CTAs greedily: each tile goes to the CTA with
+// the least work so far (blocks plus a per-tile overhead).  CTA c's tiles
+// are entries [c * stride, c * stride + stride) of *out, in order, each
+// {row = head * rows + i, blocks, b * Hq + hq, i}, ended early by blocks = -1.
+// Built on the first launch of a (units, Hq, grid, device) and cached in
+// the MaskInfo.
+bsa_status tile_schedule(const bsa_mask_info* info, int64_t units, int32_t hq, int32_t grid, const int4** out,
+                         int32_t* stride);
 
 // Programmatic dependent launch: a kernel launched this way may start (its
 // set-up: barriers, tensor memory, descriptor prefetch) while the previous

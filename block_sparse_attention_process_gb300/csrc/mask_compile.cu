@@ -566,6 +566,12 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
                                      static_cast<int32_t*>(hist.p), info->row_order);
   BSA_CK(cudaGetLastError(), "order_rows launch");
   BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
+  info->row_len_h.resize(static_cast<size_t>(n_rows));
+  info->row_order_h.resize(static_cast<size_t>(n_rows));
+  BSA_CK(cudaMemcpy(info->row_len_h.data(), info->row_len, n_rows * sizeof(int32_t), cudaMemcpyDeviceToHost),
+         "copy row_len");
+  BSA_CK(cudaMemcpy(info->row_order_h.data(), info->row_order, n_rows * sizeof(int32_t), cudaMemcpyDeviceToHost),
+         "copy row_order");
 #undef BSA_CK
   guard.keep = true;
   *out = info;

@@ -122,9 +122,11 @@ typedef struct {
 /* Compile a mask into MaskInfo ("What is MaskInfo in splash attention?",
  * "What does grid shrinking do in splash attention?").  Runs the classifier,
  * the partial-block dedup (dense masks only), the next-block pass, the
- * shrink pass and the integer downcast as kernels on `stream`, then
- * synchronises `stream` once to size the outputs.  *out receives a new
- * handle on success and is untouched on failure. */
+ * shrink pass and the integer downcast as kernels on `stream`, synchronising
+ * `stream` to size the outputs and again before returning: the MaskInfo is
+ * complete on return, and the attention kernels read it without waiting for
+ * earlier work on their stream.  *out receives a new handle on success and
+ * is untouched on failure. */
 BSA_API bsa_status bsa_mask_compile(const bsa_mask_spec* spec, const bsa_mask_opts* opts, bsa_stream stream,
                             bsa_mask_info** out);
 BSA_API bsa_status bsa_mask_info_view(const bsa_mask_info* info, bsa_mask_info_desc* out);
