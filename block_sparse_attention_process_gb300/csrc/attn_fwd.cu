@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_s = [&]() -> bool {
       const uint32_t ks = s_cnt % kStagesK;
       if (!mbar_wait_warp(&s.k_full[ks], (s_cnt / kStagesK) & 1u, wc)) return false;
-      const uint32_t info = s.binfo[s_cnt % kInfoRing].x;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[s_cnt % kInfoRing].x, 0);
       if (info & kEnd) {
         s_end = true;
         return true;
@@ -333,11 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (info & kFirst) {  // first block of a tile: its Q buffer
         const uint32_t qb = q_uses & 1u;
         if (!mbar_wait_warp(&s.q_full[qb], (q_uses >> 1) & 1u, wc)) return false;
-        cur_q = qdesc0 + qb * kTileDesc;
+        cur_q = qb ? qdesc0 + kTileDesc : qdesc0;
       }
       tc_fence_after();
       const uint32_t sb = s_cnt % kSBufs;
-      const uint64_t kd = kdesc0 + ks * kTileDesc;
+      const uint64_t kd = ks ? kdesc0 + kTileDesc : kdesc0;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
