@@ -830,30 +830,56 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dkv_decode(p, T).total);
     uint32_t kv_uses = 0, acc_uses = 0;
     bool ok = true;
-    for (uint32_t n = 0; ok && n < total; ++n) {
-      const uint32_t st = n % kDkvStages;
-      if (!mbar_wait_warp(&s.in_full[st], (n / kDkvStages) & 1u, wc)) { ok = false; break; }
-      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[n % kInfoRing].x, 0);
-      const bool first = (info >> 20) & 1u, last = (info >> 21) & 1u;
-      if (first) {
-        if (!mbar_wait_warp(&s.kv_full, kv_uses & 1u, wc)) { ok = false; break; }
+    // S^T(n+1) is issued right after dV(n) (which reads P^T(n) from the same
+    // columns first), so the tensor cores compute the next scores while the
+    // elementwise warps work on dS^T(n); dP^T(n+1) follows dK(n) likewise.
+    // Order: S^T(0) dP^T(0) | dV(0) S^T(1) dK(0) dP^T(1) | dV(1) S^T(2) ...
+    uint32_t flags = 0;  // first/last bits of items n and n+1, two per item
+    auto item_flags = [&](uint32_t k) -> bool {
+      const uint32_t st = k % kDkvStages;
+      if (!mbar_wait_warp(&s.in_full[st], (k / kDkvStages) & 1u, wc)) return false;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[k % kInfoRing].x, 0);
+      const uint32_t sh = 2u * (k & 7u);
+      flags = (flags & ~(3u << sh)) | (((info >> 20) & 3u) << sh);
+      if ((info >> 20) & 1u) {  // first item of a tile: its K and V
+        if (!mbar_wait_warp(&s.kv_full, kv_uses & 1u, wc)) return false;
         ++kv_uses;
       }
       tc_fence_after();
-      const uint64_t qd = qdesc0 + st * kTileDesc, dod = dodesc0 + st * kTileDesc;
+      return true;
+    };
+    auto issue_st = [&](uint32_t k) {
+      const uint64_t qd = qdesc0 + (k % kDkvStages) * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
         mma_ss_elect(tmem + kDkvColST, kdesc + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.st_full);
+    };
+    auto issue_dpt = [&](uint32_t k) {
+      const uint64_t dod = dodesc0 + (k % kDkvStages) * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
         mma_ss_elect(tmem + kDkvColDP, vdesc + off, dod + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.dpt_full);
-      if (last) mma_commit_elect(&s.kv_empty);  // K and V are read by the S^T / dP^T MMAs only
+      // K and V are read by the S^T / dP^T MMAs only
+      if ((flags >> (2u * (k & 7u))) & 2u) mma_commit_elect(&s.kv_empty);
+    };
+    if (total > 0) {
+      ok = item_flags(0);
+      if (ok) {
+        issue_st(0);
+        issue_dpt(0);
+      }
+    }
+    for (uint32_t n = 0; ok && n < total; ++n) {
+      const uint32_t st = n % kDkvStages;
+      const uint32_t fl = (flags >> (2u * (n & 7u))) & 3u;
+      const bool first = fl & 1u, last = fl & 2u;
+      const bool more = n + 1 < total;
       // dV += P^T dO
       if (!mbar_wait_warp(&s.p_full, n & 1u, wc)) { ok = false; break; }
       if (first && acc_uses > 0 && !mbar_wait_warp(&s.acc_empty, (acc_uses - 1) & 1u, wc)) { ok = false; break; }
@@ -864,6 +890,11 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         mma_ts_elect(tmem + kDkvColDV, tmem + kDkvColST + part_a_col<DkvShape<D>::kCols>(kk),
                      domn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
+      // next item's S^T over the P^T columns the dV MMA has just read
+      if (more) {
+        if (!item_flags(n + 1)) { ok = false; break; }
+        issue_st(n + 1);
+      }
       // dK += dS^T Q
       if (!mbar_wait_warp(&s.ds_full, n & 1u, wc)) { ok = false; break; }
       tc_fence_after();
@@ -878,6 +909,8 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         mma_commit_elect(&s.acc_full);
         ++acc_uses;
       }
+      // next item's dP^T over the dS^T columns the dK MMA has just read
+      if (more) issue_dpt(n + 1);
     }
     mma_commit_elect(&s.drain);
     uint32_t dummy_abort = 0;
