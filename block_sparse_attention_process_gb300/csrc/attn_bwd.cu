@@ -75,6 +75,10 @@ struct BwdParams {
   int32_t grad_fp32;
   MaskInfoDev mi;
   int32_t n_tiles;
+  // this launch's tile lists (sched_stride entries per CTA), or null for
+  // round-robin tiles in longest-first order
+  const int4* sched;
+  int32_t sched_stride;
   uint32_t* err;
   uint64_t wait_ns;
 };
@@ -213,21 +217,41 @@ __device__ __forceinline__ DqTile dq_decode(const BwdParams& p, int32_t T) {
   return t;
 }
 
+// The k-th tile of this CTA, from the launch's schedule (or round-robin);
+// false past the last one.
+__device__ __forceinline__ bool dq_tile(const BwdParams& p, int32_t k, DqTile& t) {
+  if (p.sched) {
+    if (k >= p.sched_stride) return false;
+    const int4 te = p.sched[static_cast<int64_t>(blockIdx.x) * p.sched_stride + k];
+    if (te.y < 0) return false;
+    t.i = te.x;
+    t.n = te.y;
+    t.b = te.z / p.Hq;
+    t.hq = te.z % p.Hq;
+    t.hm = p.mi.heads == 1 ? 0 : t.hq;
+    t.row_base = (static_cast<int64_t>(t.hm) * p.mi.rows + t.i) * p.mi.width;
+    return true;
+  }
+  const int64_t T = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(k) * gridDim.x;
+  if (T >= p.n_tiles) return false;
+  t = dq_decode(p, static_cast<int32_t>(T));
+  return true;
+}
+
 // Cursor over the CTA's (tile, block) sequence of the dQ launch (tiles
 // without blocks skipped; each tile yields exactly row_len blocks).
 struct DqSeq {
-  int32_t T, j, pos;
+  int32_t k, j, pos;
   DqTile t;
   RawRef ahead;
   bool valid;
   __device__ __forceinline__ void start_tile(const BwdParams& p) {
     while (true) {
-      T += gridDim.x;
-      if (T >= p.n_tiles) {
+      ++k;
+      if (!dq_tile(p, k, t)) {
         valid = false;
         return;
       }
-      t = dq_decode(p, T);
       if (t.n > 0) break;
     }
     j = 0;
@@ -236,7 +260,7 @@ struct DqSeq {
     valid = true;
   }
   __device__ __forceinline__ void init(const BwdParams& p) {
-    T = static_cast<int32_t>(blockIdx.x) - static_cast<int32_t>(gridDim.x);
+    k = -1;
     start_tile(p);
   }
   __device__ __forceinline__ bool next(const BwdParams& p, BlockRef& br, bool& first, bool& last) {
@@ -406,7 +430,10 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
     const uint64_t kmn0 = sdesc_sw128(smem_u32(s.k[0]), 16384, 1024);
     const uint64_t vdesc0 = sdesc_sw128(smem_u32(s.v[0]), 16, 1024);
     uint32_t total = 0;
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dq_decode(p, T).n);
+    {
+      DqTile t;
+      for (int32_t kt = 0; dq_tile(p, kt, t); ++kt) total += static_cast<uint32_t>(t.n);
+    }
     uint32_t s_cnt = 0, dp_cnt = 0, q_uses = 0, acc_uses = 0;
     bool ok = true;
     auto k_ready = [&](uint32_t n) -> bool {
@@ -491,14 +518,16 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
     const float scale_log2 = p.scale_log2;
     uint32_t n = 0, acc_uses = 0;
     bool ok = true;
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) {
-      const DqTile t = dq_decode(p, T);
-      if (t.n > 0) continue;
-      const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
-      store_zero_cols(p.dq, p.grad_fp32, qrow, D, part * kPartD, kPartD);
-    }
     uint32_t total = 0;
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dq_decode(p, T).n);
+    {
+      DqTile t;
+      for (int32_t kt = 0; dq_tile(p, kt, t); ++kt) {
+        total += static_cast<uint32_t>(t.n);
+        if (t.n > 0) continue;
+        const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + t.hq) * p.Sq + static_cast<int64_t>(t.i) * 128 + r;
+        store_zero_cols(p.dq, p.grad_fp32, qrow, D, part * kPartD, kPartD);
+      }
+    }
     float lse2 = 0.f, dsum_r = 0.f;
     int64_t lo = 0, hi = 0, qrow = 0;
     uint32_t tiles = 0;
@@ -655,6 +684,25 @@ __device__ __forceinline__ DkvTile dkv_decode(const BwdParams& p, int32_t T) {
   return t;
 }
 
+// The k-th tile of this CTA, from the launch's schedule (or round-robin);
+// false past the last one.
+__device__ __forceinline__ bool dkv_tile(const BwdParams& p, int32_t k, DkvTile& t) {
+  if (p.sched) {
+    if (k >= p.sched_stride) return false;
+    const int4 te = p.sched[static_cast<int64_t>(blockIdx.x) * p.sched_stride + k];
+    if (te.y < 0) return false;
+    t.j = te.x;
+    t.total = te.y;
+    t.b = te.z / p.Hkv;
+    t.g = te.z % p.Hkv;
+    return true;
+  }
+  const int64_t T = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(k) * gridDim.x;
+  if (T >= p.n_tiles) return false;
+  t = dkv_decode(p, static_cast<int32_t>(T));
+  return true;
+}
+
 // Items of one dK/dV tile, in order: q heads of the group, then the
 // non-empty query blocks of that head's MaskInfo row (each yields exactly
 // row_len blocks; a malformed row is padded with flagged dummy blocks).
@@ -763,8 +811,8 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       const uint64_t pol_q = policy_evict_last();
       uint32_t kv_loads = 0, in_loads = 0;
       bool ok = true;
-      for (int32_t T = blockIdx.x; T < p.n_tiles && ok; T += gridDim.x) {
-        const DkvTile t = dkv_decode(p, T);
+      DkvTile t;
+      for (int32_t kt = 0; ok && dkv_tile(p, kt, t); ++kt) {
         if (t.total == 0) continue;
         if (kv_loads >= 1 && !mbar_wait(&s.kv_empty, (kv_loads - 1) & 1u, wc)) { ok = false; break; }
         mbar_arrive_expect_tx(&s.kv_full, 2 * kTile);
@@ -775,8 +823,8 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         }
         ++kv_loads;
         // warm L2 with this CTA's next tile's K and V
-        for (int32_t T2 = T + static_cast<int32_t>(gridDim.x); T2 < p.n_tiles; T2 += gridDim.x) {
-          const DkvTile t2 = dkv_decode(p, T2);
+        DkvTile t2;
+        for (int32_t k2 = kt + 1; dkv_tile(p, k2, t2); ++k2) {
           if (t2.total == 0) continue;
           const int64_t row2 = (static_cast<int64_t>(t2.b) * p.Hkv + t2.g) * p.Skv + t2.j * 128;
           prefetch_l2(static_cast<const uint8_t*>(p.kp) + row2 * D * 2, 128 * D * 2);
@@ -827,7 +875,10 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     const uint64_t dodesc0 = sdesc_sw128(smem_u32(s.dout[0]), 16, 1024);
     const uint64_t domn0 = sdesc_sw128(smem_u32(s.dout[0]), 16384, 1024);
     uint32_t total = 0;
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dkv_decode(p, T).total);
+    {
+      DkvTile t;
+      for (int32_t kt = 0; dkv_tile(p, kt, t); ++kt) total += static_cast<uint32_t>(t.total);
+    }
     uint32_t kv_uses = 0, acc_uses = 0;
     bool ok = true;
     // S^T(n+1) is issued right after dV(n) (which reads P^T(n) from the same
@@ -927,15 +978,17 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t col0 = static_cast<uint32_t>(part) * kCols;  // query columns of this part
     bool ok = true;
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) {
-      const DkvTile t = dkv_decode(p, T);
-      if (t.total > 0) continue;
-      const int64_t krow = (static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + static_cast<int64_t>(t.j) * 128 + r;
-      store_zero_cols(p.dk, p.grad_fp32, krow, D, part * kPartD, kPartD);
-      store_zero_cols(p.dv, p.grad_fp32, krow, D, part * kPartD, kPartD);
-    }
     uint32_t total = 0;
-    for (int32_t T = blockIdx.x; T < p.n_tiles; T += gridDim.x) total += static_cast<uint32_t>(dkv_decode(p, T).total);
+    {
+      DkvTile t;
+      for (int32_t kt = 0; dkv_tile(p, kt, t); ++kt) {
+        total += static_cast<uint32_t>(t.total);
+        if (t.total > 0) continue;
+        const int64_t krow = (static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + static_cast<int64_t>(t.j) * 128 + r;
+        store_zero_cols(p.dk, p.grad_fp32, krow, D, part * kPartD, kPartD);
+        store_zero_cols(p.dv, p.grad_fp32, krow, D, part * kPartD, kPartD);
+      }
+    }
     uint32_t acc_uses = 0;
     int64_t lo = 0, hi = 0, krow = 0;
     const uint64_t nsc2 = f2_pack(-p.scale, -p.scale), nl2e2 = f2_pack(-kLog2e, -kLog2e);
@@ -1097,7 +1150,7 @@ BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
 
 template <int D>
 bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
-                      uint32_t* err) {
+                      uint32_t* err, bool schedule) {
   CUtensorMap tq, tk, tv, tdo;
   if (!make_maps(a, &tq, &tk, &tv, &tdo)) return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor");
   BwdParams p = make_params(a, info, scale, err);
@@ -1111,6 +1164,10 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
+  if (schedule) {
+    bsa_status st = tile_schedule(info, a->B, a->Hkv, a->Hq / a->Hkv, grid, &p.sched, &p.sched_stride);
+    if (st != BSA_OK) return st;
+  }
   cudaError_t e = launch_kernel(dkv_kernel<D>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dkv launch");
@@ -1119,7 +1176,7 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
 
 template <int D>
 bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
-                     uint32_t* err) {
+                     uint32_t* err, bool schedule) {
   CUtensorMap tq, tk, tv, tdo;
   if (!make_maps(a, &tq, &tk, &tv, &tdo)) return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor");
   BwdParams p = make_params(a, info, scale, err);
@@ -1133,6 +1190,10 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
+  if (schedule) {
+    bsa_status st = tile_schedule(info, a->B, a->Hq, 1, grid, &p.sched, &p.sched_stride);
+    if (st != BSA_OK) return st;
+  }
   cudaError_t e = launch_kernel(dq_kernel<D>, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dq launch");
@@ -1142,15 +1203,15 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
 }  // namespace
 
 bsa_status dkv_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
-                      uint32_t* err) {
-  if (a->D == 128) return launch_dkv<128>(a, info, scale, stream, err);
-  return launch_dkv<64>(a, info, scale, stream, err);
+                      uint32_t* err, bool schedule) {
+  if (a->D == 128) return launch_dkv<128>(a, info, scale, stream, err, schedule);
+  return launch_dkv<64>(a, info, scale, stream, err, schedule);
 }
 
 bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
-                     uint32_t* err) {
-  if (a->D == 128) return launch_dq<128>(a, info, scale, stream, err);
-  return launch_dq<64>(a, info, scale, stream, err);
+                     uint32_t* err, bool schedule) {
+  if (a->D == 128) return launch_dq<128>(a, info, scale, stream, err, schedule);
+  return launch_dq<64>(a, info, scale, stream, err, schedule);
 }
 
 }  // namespace bsa

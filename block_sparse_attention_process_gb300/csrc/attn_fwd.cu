@@ -187,16 +187,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n;
       return true;
     };
-    // this CTA's tiles: {MaskInfo row, blocks, b * Hq + hq, query block}, next one loaded ahead
+    // this CTA's tiles: {query block, blocks, b * Hq + hq}, next one loaded ahead
     const int4* mine = p.sched + static_cast<int64_t>(blockIdx.x) * p.sched_stride;
     int4 ahead_tile = mine[0];
     for (int32_t k = 0; ok && k < p.sched_stride; ++k) {
       const int4 te = ahead_tile;
       if (te.y < 0) break;
       if (k + 1 < p.sched_stride) ahead_tile = mine[k + 1];
-      const int32_t t_n = te.y, t_i = te.w;
+      const int32_t t_n = te.y, t_i = te.x;
       const int32_t t_b = te.z / p.Hq, t_hq = te.z % p.Hq;
-      const int64_t t_row_base = static_cast<int64_t>(te.x) * p.mi.width;
+      const int32_t t_hm = p.mi.heads == 1 ? 0 : t_hq;
+      const int64_t t_row_base = (static_cast<int64_t>(t_hm) * p.mi.rows + t_i) * p.mi.width;
       const int64_t out_row = static_cast<int64_t>(te.z) * p.Sq + static_cast<int64_t>(t_i) * 128;
       if (t_n == 0) {
         // every key masked for the whole query block: O = 0, LSE = -inf
@@ -679,8 +680,7 @@ bsa_status launch_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, float sc
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  const int64_t units = info->heads == 1 ? static_cast<int64_t>(a->B) * a->Hq : a->B;
-  bsa_status st = tile_schedule(info, units, a->Hq, grid, &p.sched, &p.sched_stride);
+  bsa_status st = tile_schedule(info, a->B, a->Hq, 1, grid, &p.sched, &p.sched_stride);
   if (st != BSA_OK) return st;
   cudaError_t e = launch_kernel(fwd_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p);
   if (e == cudaSuccess) e = cudaGetLastError();

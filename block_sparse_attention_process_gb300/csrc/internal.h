@@ -29,8 +29,7 @@ struct bsa_mask_info {
   std::vector<int32_t> row_len_h, row_order_h;
   // tile schedules built so far (device memory, freed with the handle)
   struct Schedule {
-    int64_t units = 0;
-    int32_t hq = 0, grid = 0, device = -1, stride = 0;
+    int32_t n_b = 0, n_g = 0, group = 0, grid = 0, device = -1, stride = 0;
     int4* dev = nullptr;
   };
   mutable std::vector<Schedule> schedules;
@@ -52,25 +51,28 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
                              bsa_mask_info** out);
 bsa_status fwd_launch(const bsa_fwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream);
 bsa_status rowsum_launch(const bsa_bwd_args* a, cudaStream_t stream);
-// `err` (optional) replaces the library's device error word for this launch.
+// `err` (optional) replaces the library's device error word for this launch;
+// `schedule` false hands tiles out round-robin instead of building (and
+// allocating) a tile schedule.
 bsa_status dkv_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
-                      uint32_t* err = nullptr);
+                      uint32_t* err = nullptr, bool schedule = true);
 bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
-                     uint32_t* err = nullptr);
+                     uint32_t* err = nullptr, bool schedule = true);
 bsa_status debug_wait_timeout_launch(cudaStream_t stream);
 
 int num_sms();
 
-// Work tiles of a launch: every MaskInfo row (row_order order, longest
-// first) times `units` (B * Hq for a shared mask, B for per-head masks),
-// handed to `grid` persistent CTAs greedily: each tile goes to the CTA with
-// the least work so far (blocks plus a per-tile overhead).  CTA c's tiles
-// are entries [c * stride, c * stride + stride) of *out, in order, each
-// {row = head * rows + i, blocks, b * Hq + hq, i}, ended early by blocks = -1.
-// Built on the first launch of a (units, Hq, grid, device) and cached in
-// the MaskInfo.
-bsa_status tile_schedule(const bsa_mask_info* info, int64_t units, int32_t hq, int32_t grid, const int4** out,
-                         int32_t* stride);
+// Work tiles of a launch: (b, g, MaskInfo row i) for b < n_b, g < n_g, each
+// covering `group` mask heads (the q heads of a KV group in the dK/dV
+// launch; 1 in the forward and dQ launches), handed to `grid` persistent
+// CTAs greedily, longest first: each tile goes to the CTA with the least
+// work so far (blocks plus a per-tile overhead).  CTA c's tiles are entries
+// [c * stride, c * stride + stride) of *out, in order, each
+// {i, blocks over the group, b * n_g + g, 0}, ended early by blocks = -1.
+// Built on the first launch of a (n_b, n_g, group, grid, device) and cached
+// in the MaskInfo.
+bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t grid,
+                         const int4** out, int32_t* stride);
 
 // Programmatic dependent launch: a kernel launched this way may start (its
 // set-up: barriers, tensor memory, descriptor prefetch) while the previous

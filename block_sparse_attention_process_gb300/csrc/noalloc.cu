@@ -108,7 +108,8 @@ extern "C" bsa_status bsa_bwd_noalloc(const bsa_bwd_args* a, const bsa_mask_info
   const float scale = std::isnan(a->softmax_scale) ? 1.0f / std::sqrt(static_cast<float>(a->D)) : a->softmax_scale;
   s = rowsum_launch(&b, st);
   if (s != BSA_OK) return s;
-  s = dkv_launch(&b, dkv_info, scale, st, err);
+  // round-robin tiles: a launch-time tile schedule would allocate
+  s = dkv_launch(&b, dkv_info, scale, st, err, false);
   if (s != BSA_OK) return s;
-  return dq_launch(&b, fwd_info, scale, st, err);
+  return dq_launch(&b, fwd_info, scale, st, err, false);
 }

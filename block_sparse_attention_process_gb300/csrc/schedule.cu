@@ -15,41 +15,55 @@
 
 namespace bsa {
 
-bsa_status tile_schedule(const bsa_mask_info* info, int64_t units, int32_t hq, int32_t grid, const int4** out,
-                         int32_t* stride) {
+bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t grid,
+                         const int4** out, int32_t* stride) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   std::lock_guard<std::mutex> lk(info->sched_mu);
   for (const auto& sc : info->schedules)
-    if (sc.units == units && sc.hq == hq && sc.grid == grid && sc.device == dev) {
+    if (sc.n_b == n_b && sc.n_g == n_g && sc.group == group && sc.grid == grid && sc.device == dev) {
       *out = sc.dev;
       *stride = sc.stride;
       return BSA_OK;
     }
-  const int64_t n_rows = static_cast<int64_t>(info->row_order_h.size());
-  const int64_t n_tiles = n_rows * units;
-  if (grid <= 0 || n_tiles <= 0) return fail(BSA_ERR_INVALID_ARG, "empty tile schedule");
-  // greedy over tiles in longest-first order; cost in eighths of a block,
-  // with a per-tile overhead of about one and a half blocks
+  const int32_t rows = info->rows;
+  if (grid <= 0 || rows <= 0 || n_b <= 0 || n_g <= 0 || group <= 0) return fail(BSA_ERR_INVALID_ARG, "empty tile schedule");
+  // tiles in longest-first order: {row, blocks, b * n_g + g}
+  struct T {
+    int32_t i, n, bg;
+  };
+  std::vector<T> tiles;
+  tiles.reserve(static_cast<size_t>(rows) * n_b * n_g);
+  if (info->heads == 1) {
+    // rows by decreasing length (row_order), each for every (b, g)
+    for (int32_t rank = 0; rank < rows; ++rank) {
+      const int32_t i = info->row_order_h[static_cast<size_t>(rank)];
+      const int32_t n = info->row_len_h[static_cast<size_t>(i)] * group;
+      for (int32_t bg = 0; bg < n_b * n_g; ++bg) tiles.push_back({i, n, bg});
+    }
+  } else {
+    // per-head masks: tile (b, g, i) covers mask heads g*group .. g*group+group-1 of row i
+    for (int32_t g = 0; g < n_g; ++g)
+      for (int32_t i = 0; i < rows; ++i) {
+        int32_t n = 0;
+        for (int32_t gh = 0; gh < group; ++gh) n += info->row_len_h[static_cast<size_t>((g * group + gh) * rows + i)];
+        for (int32_t b = 0; b < n_b; ++b) tiles.push_back({i, n, b * n_g + g});
+      }
+    std::stable_sort(tiles.begin(), tiles.end(), [](const T& x, const T& y) { return x.n > y.n; });
+  }
+  // greedy; cost in eighths of a block, with a per-tile overhead of about
+  // one and a half blocks
   std::vector<std::vector<int4>> lists(static_cast<size_t>(grid));
   using Load = std::pair<int64_t, int32_t>;  // (work so far, CTA): ties go to the lower CTA
   std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
   for (int32_t c = 0; c < grid; ++c) heap.push({0, c});
-  for (int64_t rank = 0; rank < n_rows; ++rank) {
-    const int32_t row = info->row_order_h[static_cast<size_t>(rank)];
-    const int32_t n = info->row_len_h[static_cast<size_t>(row)];
-    const int32_t i = row % info->rows;
-    const int32_t hm = row / info->rows;
-    for (int64_t u = 0; u < units; ++u) {
-      // shared mask: u = b * Hq + hq; per-head masks: u = b and hq = the mask head
-      const int32_t bh = info->heads == 1 ? static_cast<int32_t>(u) : static_cast<int32_t>(u) * hq + hm;
-      Load top = heap.top();
-      heap.pop();
-      lists[static_cast<size_t>(top.second)].push_back(make_int4(row, n, bh, i));
-      top.first += 8 * static_cast<int64_t>(n) + 12;
-      heap.push(top);
-    }
+  for (const T& t : tiles) {
+    Load top = heap.top();
+    heap.pop();
+    lists[static_cast<size_t>(top.second)].push_back(make_int4(t.i, t.n, t.bg, 0));
+    top.first += 8 * static_cast<int64_t>(t.n) + 12;
+    heap.push(top);
   }
   size_t longest = 0;
   for (const auto& l : lists) longest = std::max(longest, l.size());
@@ -67,8 +81,9 @@ bsa_status tile_schedule(const bsa_mask_info* info, int64_t units, int32_t hq, i
     return cuda_fail(e, "upload tile schedule");
   }
   bsa_mask_info::Schedule sc;
-  sc.units = units;
-  sc.hq = hq;
+  sc.n_b = n_b;
+  sc.n_g = n_g;
+  sc.group = group;
   sc.grid = grid;
   sc.device = dev;
   sc.stride = st;
