@@ -44,6 +44,43 @@ uint32_t* device_error_word() {
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns; }
 
+namespace {
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[64] = {};
+}  // namespace
+
+bsa_status pool_alloc(void** p, size_t bytes, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(BSA_ERR_UNSUPPORTED, "device index above 63");
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pools[dev]) {
+      cudaMemPoolProps props{};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      e = cudaMemPoolCreate(&g_pools[dev], &props);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+      uint64_t keep = UINT64_MAX;  // keep freed memory for the next call
+      cudaMemPoolSetAttribute(g_pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    pool = g_pools[dev];
+  }
+  e = cudaMallocFromPoolAsync(p, bytes, pool, stream);
+  if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? fail(BSA_ERR_OOM, "workspace allocation failed")
+                                                              : cuda_fail(e, "cudaMallocFromPoolAsync");
+  return BSA_OK;
+}
+
+bsa_status pool_free(void* p, cudaStream_t stream) {
+  cudaError_t e = cudaFreeAsync(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+  return BSA_OK;
+}
+
 bool pdl_enabled() {
   static const bool on = [] {
     const char* e = std::getenv("BSA_PDL");

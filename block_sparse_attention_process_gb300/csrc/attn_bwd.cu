@@ -79,6 +79,13 @@ struct BwdParams {
   // round-robin tiles in longest-first order
   const int4* sched;
   int32_t sched_stride;
+  // dK/dV launch with the q heads of a group split over kv_splits CTAs:
+  // each writes fp32 partial sums at row split * part_rows + key row of
+  // part_dk / part_dv, summed afterwards (kv_splits == 1: direct output)
+  int32_t kv_splits;
+  int64_t part_rows;
+  float* part_dk;
+  float* part_dv;
   uint32_t* err;
   uint64_t wait_ns;
 };
@@ -657,7 +664,8 @@ struct __align__(1024) DkvSmem {
 
 struct DkvTile {
   int32_t b, g, j;
-  int32_t total;  // non-empty blocks over the group's q heads
+  int32_t total;  // non-empty blocks over the q heads of this tile's split of the group
+  int32_t split;
 };
 
 __device__ __forceinline__ int32_t dkv_mask_head(const BwdParams& p, int32_t hq) {
@@ -673,12 +681,14 @@ __device__ __forceinline__ DkvTile dkv_decode(const BwdParams& p, int32_t T) {
     t.b = bg / p.Hkv;
     t.g = bg % p.Hkv;
     t.total = p.mi.row_len[t.j] * G;
+    t.split = 0;
   } else {
     t.j = T % p.nK;
     const int32_t bg = T / p.nK;
     t.b = bg / p.Hkv;
     t.g = bg % p.Hkv;
     t.total = 0;
+    t.split = 0;
     for (int32_t gh = 0; gh < G; ++gh) t.total += p.mi.row_len[(t.g * G + gh) * p.mi.rows + t.j];
   }
   return t;
@@ -695,6 +705,7 @@ __device__ __forceinline__ bool dkv_tile(const BwdParams& p, int32_t k, DkvTile&
     t.total = te.y;
     t.b = te.z / p.Hkv;
     t.g = te.z % p.Hkv;
+    t.split = te.w;
     return true;
   }
   const int64_t T = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(k) * gridDim.x;
@@ -703,16 +714,22 @@ __device__ __forceinline__ bool dkv_tile(const BwdParams& p, int32_t k, DkvTile&
   return true;
 }
 
+// Row of a tile's first key in the dK/dV output (or in the partial sums of
+// its split).
+__device__ __forceinline__ int64_t dkv_out_row(const BwdParams& p, const DkvTile& t, int64_t krow) {
+  return p.kv_splits > 1 ? static_cast<int64_t>(t.split) * p.part_rows + krow : krow;
+}
+
 // Items of one dK/dV tile, in order: q heads of the group, then the
 // non-empty query blocks of that head's MaskInfo row (each yields exactly
 // row_len blocks; a malformed row is padded with flagged dummy blocks).
 struct DkvItems {
-  int32_t gh, n, j, pos;
+  int32_t gh, gh_end, n, j, pos;
   int64_t row_base;
   RawRef ahead;
   __device__ __forceinline__ void start_head(const BwdParams& p, const DkvTile& t) {
     const int32_t G = p.Hq / p.Hkv;
-    while (gh < G) {
+    while (gh < gh_end) {
       const int32_t hm = dkv_mask_head(p, t.g * G + gh);
       row_base = (static_cast<int64_t>(hm) * p.mi.rows + t.j) * p.mi.width;
       n = p.mi.row_len[hm * p.mi.rows + t.j];
@@ -721,15 +738,17 @@ struct DkvItems {
     }
     j = 0;
     pos = 0;
-    if (gh < G && p.mi.width > 0) ahead = load_block(p.mi, row_base, 0);
+    if (gh < gh_end && p.mi.width > 0) ahead = load_block(p.mi, row_base, 0);
   }
   __device__ __forceinline__ void init(const BwdParams& p, const DkvTile& t) {
-    gh = 0;
+    const int32_t gs = p.Hq / p.Hkv / p.kv_splits;  // q heads of one split
+    gh = t.split * gs;
+    gh_end = gh + gs;
     start_head(p, t);
   }
   __device__ __forceinline__ bool next(const BwdParams& p, const DkvTile& t, int32_t& hq, BlockRef& br) {
     const int32_t G = p.Hq / p.Hkv;
-    if (gh >= G) return false;
+    if (gh >= gh_end) return false;
     bool found = false;
     while (pos < p.mi.width) {
       const RawRef cur = ahead;
@@ -842,7 +861,8 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           const uint32_t extra = p.mi.kind == BSA_MASK_DENSE ? static_cast<uint32_t>(br.slot)
                                                              : static_cast<uint32_t>(p.mi.q_sequence[br.col * 128]);
           s.binfo[in_loads % kInfoRing] = make_uint4(pack_info(br.col, br.label, x == 0, x == t.total - 1), extra,
-                                                     static_cast<uint32_t>(t.j * 128), static_cast<uint32_t>(krow));
+                                                     static_cast<uint32_t>(t.j * 128),
+                                                     static_cast<uint32_t>(dkv_out_row(p, t, krow)));
           mbar_arrive_expect_tx(&s.in_full[st], 2 * kTile + 1024);
           const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + hq) * p.Sq + br.col * 128;
           for (int c = 0; c < kChunks; ++c) {
@@ -984,9 +1004,11 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       for (int32_t kt = 0; dkv_tile(p, kt, t); ++kt) {
         total += static_cast<uint32_t>(t.total);
         if (t.total > 0) continue;
-        const int64_t krow = (static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + static_cast<int64_t>(t.j) * 128 + r;
-        store_zero_cols(p.dk, p.grad_fp32, krow, D, part * kPartD, kPartD);
-        store_zero_cols(p.dv, p.grad_fp32, krow, D, part * kPartD, kPartD);
+        const int64_t krow =
+            dkv_out_row(p, t, (static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + static_cast<int64_t>(t.j) * 128) + r;
+        const bool sp = p.kv_splits > 1;
+        store_zero_cols(sp ? p.part_dk : p.dk, sp ? 1 : p.grad_fp32, krow, D, part * kPartD, kPartD);
+        store_zero_cols(sp ? p.part_dv : p.dv, sp ? 1 : p.grad_fp32, krow, D, part * kPartD, kPartD);
       }
     }
     uint32_t acc_uses = 0;
@@ -1093,11 +1115,12 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         tmem_ld32(tmem + kDkvColDV + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
         reg_fence32(v);
-        store_row(p.dv, p.grad_fp32, krow, D, v, part * kPartD + c * 32, 1.f);
+        const bool sp = p.kv_splits > 1;
+        store_row(sp ? p.part_dv : p.dv, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD + c * 32, 1.f);
         tmem_ld32(tmem + kDkvColDK + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
         reg_fence32(v);
-        store_row(p.dk, p.grad_fp32, krow, D, v, part * kPartD + c * 32, p.scale);
+        store_row(sp ? p.part_dk : p.dk, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD + c * 32, p.scale);
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty);
@@ -1113,6 +1136,31 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
   }
 }
 
+// dK, dV = sums of the splits' fp32 partials (fixed order, so the result
+// does not depend on timing).  HBM-bound: 4 floats per thread and pass.
+__global__ void __launch_bounds__(256) dkv_reduce_kernel(const float4* __restrict__ pk, const float4* __restrict__ pv,
+                                                         void* dk, void* dv, int64_t n4, int64_t part4, int32_t splits,
+                                                         int32_t fp32) {
+  griddep_launch_dependents();
+  griddep_wait();  // the partials come from the dK/dV kernel
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = __ldcs(pk + i), b = __ldcs(pv + i);
+    for (int32_t sp = 1; sp < splits; ++sp) {
+      const float4 x = __ldcs(pk + sp * part4 + i), y = __ldcs(pv + sp * part4 + i);
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+    }
+    if (fp32) {
+      static_cast<float4*>(dk)[i] = a;
+      static_cast<float4*>(dv)[i] = b;
+    } else {
+      static_cast<uint2*>(dk)[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+      static_cast<uint2*>(dv)[i] = make_uint2(pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+    }
+  }
+}
+
 bool make_maps(const bsa_bwd_args* a, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tdo) {
   const uint64_t q_rows = static_cast<uint64_t>(a->B) * a->Hq * a->S_q;
   const uint64_t kv_rows = static_cast<uint64_t>(a->B) * a->Hkv * a->S_kv;
@@ -1125,6 +1173,7 @@ bool make_maps(const bsa_bwd_args* a, CUtensorMap* tq, CUtensorMap* tk, CUtensor
 
 BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, uint32_t* err) {
   BwdParams p{};
+  p.kv_splits = 1;
   p.B = a->B;
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
@@ -1163,13 +1212,48 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
     if (e != cudaSuccess) return cuda_fail(e, "set dkv smem size");
     attr_set = true;
   }
-  const int grid = std::min(p.n_tiles, num_sms());
+  // With few KV tiles (MQA, short sequences) the q heads of a group are
+  // split over several CTAs: the smallest divisor of the group that gives
+  // two tiles per SM, whose fp32 partial sums are then added up.
+  const int32_t G = a->Hq / a->Hkv;
+  const int64_t part_rows = static_cast<int64_t>(a->B) * a->Hkv * a->S_kv;
+  int32_t splits = 1;
+  if (schedule && G > 1 && p.n_tiles < 2 * num_sms()) {
+    splits = G;
+    for (int32_t d = 2; d <= G; ++d)
+      if (G % d == 0 && static_cast<int64_t>(p.n_tiles) * d >= 2 * num_sms()) {
+        splits = d;
+        break;
+      }
+    if (splits * part_rows > static_cast<int64_t>(INT32_MAX)) splits = 1;
+  }
+  p.kv_splits = splits;
+  p.part_rows = part_rows;
+  const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(p.n_tiles) * splits, num_sms()));
   if (schedule) {
-    bsa_status st = tile_schedule(info, a->B, a->Hkv, a->Hq / a->Hkv, grid, &p.sched, &p.sched_stride);
+    bsa_status st = tile_schedule(info, a->B, a->Hkv, G, splits, grid, &p.sched, &p.sched_stride);
     if (st != BSA_OK) return st;
+  }
+  void* ws = nullptr;
+  if (splits > 1) {
+    bsa_status st = pool_alloc(&ws, 2 * static_cast<size_t>(splits) * part_rows * D * sizeof(float), stream);
+    if (st != BSA_OK) return st;
+    p.part_dk = static_cast<float*>(ws);
+    p.part_dv = p.part_dk + static_cast<size_t>(splits) * part_rows * D;
   }
   cudaError_t e = launch_kernel(dkv_kernel<D>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
   if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess && splits > 1) {
+    const int64_t n4 = part_rows * D / 4;
+    const int rgrid = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(num_sms()) * 8));
+    e = launch_kernel(dkv_reduce_kernel, dim3(rgrid), dim3(256), 0, stream, reinterpret_cast<const float4*>(p.part_dk),
+                      reinterpret_cast<const float4*>(p.part_dv), a->dk, a->dv, n4, n4, splits, a->grad_fp32);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
+  if (ws) {
+    bsa_status st = pool_free(ws, stream);
+    if (e == cudaSuccess && st != BSA_OK) return st;
+  }
   if (e != cudaSuccess) return cuda_fail(e, "dkv launch");
   return BSA_OK;
 }
@@ -1191,7 +1275,7 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
   }
   const int grid = std::min(p.n_tiles, num_sms());
   if (schedule) {
-    bsa_status st = tile_schedule(info, a->B, a->Hq, 1, grid, &p.sched, &p.sched_stride);
+    bsa_status st = tile_schedule(info, a->B, a->Hq, 1, 1, grid, &p.sched, &p.sched_stride);
     if (st != BSA_OK) return st;
   }
   cudaError_t e = launch_kernel(dq_kernel<D>, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);

@@ -680,7 +680,7 @@ bsa_status launch_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, float sc
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  bsa_status st = tile_schedule(info, a->B, a->Hq, 1, grid, &p.sched, &p.sched_stride);
+  bsa_status st = tile_schedule(info, a->B, a->Hq, 1, 1, grid, &p.sched, &p.sched_stride);
   if (st != BSA_OK) return st;
   cudaError_t e = launch_kernel(fwd_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p);
   if (e == cudaSuccess) e = cudaGetLastError();

@@ -29,7 +29,7 @@ struct bsa_mask_info {
   std::vector<int32_t> row_len_h, row_order_h;
   // tile schedules built so far (device memory, freed with the handle)
   struct Schedule {
-    int32_t n_b = 0, n_g = 0, group = 0, grid = 0, device = -1, stride = 0;
+    int32_t n_b = 0, n_g = 0, group = 0, splits = 0, grid = 0, device = -1, stride = 0;
     int4* dev = nullptr;
   };
   mutable std::vector<Schedule> schedules;
@@ -62,17 +62,23 @@ bsa_status debug_wait_timeout_launch(cudaStream_t stream);
 
 int num_sms();
 
-// Work tiles of a launch: (b, g, MaskInfo row i) for b < n_b, g < n_g, each
-// covering `group` mask heads (the q heads of a KV group in the dK/dV
-// launch; 1 in the forward and dQ launches), handed to `grid` persistent
-// CTAs greedily, longest first: each tile goes to the CTA with the least
-// work so far (blocks plus a per-tile overhead).  CTA c's tiles are entries
-// [c * stride, c * stride + stride) of *out, in order, each
-// {i, blocks over the group, b * n_g + g, 0}, ended early by blocks = -1.
-// Built on the first launch of a (n_b, n_g, group, grid, device) and cached
-// in the MaskInfo.
-bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t grid,
-                         const int4** out, int32_t* stride);
+// Work tiles of a launch: (b, g, MaskInfo row i, split) for b < n_b, g < n_g
+// and split < splits, each covering group / splits mask heads (the q heads
+// of a KV group in the dK/dV launch, split over `splits` CTAs when the
+// group is large; 1 head, 1 split in the forward and dQ launches), handed
+// to `grid` persistent CTAs greedily, longest first: each tile goes to the
+// CTA with the least work so far (blocks plus a per-tile overhead).  CTA
+// c's tiles are entries [c * stride, c * stride + stride) of *out, in
+// order, each {i, blocks, b * n_g + g, split}, ended early by blocks = -1.
+// Built on the first launch of a (n_b, n_g, group, splits, grid, device)
+// and cached in the MaskInfo.
+bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t splits,
+                         int32_t grid, const int4** out, int32_t* stride);
+
+// Stream-ordered device memory from the library's pool on the current
+// device (kept cached by the pool between calls).
+bsa_status pool_alloc(void** p, size_t bytes, cudaStream_t stream);
+bsa_status pool_free(void* p, cudaStream_t stream);
 
 // Programmatic dependent launch: a kernel launched this way may start (its
 // set-up: barriers, tensor memory, descriptor prefetch) while the previous

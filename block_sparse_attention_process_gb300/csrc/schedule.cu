@@ -15,23 +15,26 @@
 
 namespace bsa {
 
-bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t grid,
-                         const int4** out, int32_t* stride) {
+bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t splits,
+                         int32_t grid, const int4** out, int32_t* stride) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   std::lock_guard<std::mutex> lk(info->sched_mu);
   for (const auto& sc : info->schedules)
-    if (sc.n_b == n_b && sc.n_g == n_g && sc.group == group && sc.grid == grid && sc.device == dev) {
+    if (sc.n_b == n_b && sc.n_g == n_g && sc.group == group && sc.splits == splits && sc.grid == grid &&
+        sc.device == dev) {
       *out = sc.dev;
       *stride = sc.stride;
       return BSA_OK;
     }
   const int32_t rows = info->rows;
-  if (grid <= 0 || rows <= 0 || n_b <= 0 || n_g <= 0 || group <= 0) return fail(BSA_ERR_INVALID_ARG, "empty tile schedule");
-  // tiles in longest-first order: {row, blocks, b * n_g + g}
+  if (grid <= 0 || rows <= 0 || n_b <= 0 || n_g <= 0 || group <= 0 || splits <= 0 || group % splits)
+    return fail(BSA_ERR_INVALID_ARG, "empty tile schedule");
+  const int32_t gs = group / splits;  // mask heads of one split
+  // tiles in longest-first order: {row, blocks, b * n_g + g, split}
   struct T {
-    int32_t i, n, bg;
+    int32_t i, n, bg, sp;
   };
   std::vector<T> tiles;
   tiles.reserve(static_cast<size_t>(rows) * n_b * n_g);
@@ -39,17 +42,21 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
     // rows by decreasing length (row_order), each for every (b, g)
     for (int32_t rank = 0; rank < rows; ++rank) {
       const int32_t i = info->row_order_h[static_cast<size_t>(rank)];
-      const int32_t n = info->row_len_h[static_cast<size_t>(i)] * group;
-      for (int32_t bg = 0; bg < n_b * n_g; ++bg) tiles.push_back({i, n, bg});
+      const int32_t n = info->row_len_h[static_cast<size_t>(i)] * gs;
+      for (int32_t bg = 0; bg < n_b * n_g; ++bg)
+        for (int32_t sp = 0; sp < splits; ++sp) tiles.push_back({i, n, bg, sp});
     }
   } else {
-    // per-head masks: tile (b, g, i) covers mask heads g*group .. g*group+group-1 of row i
+    // per-head masks: tile (b, g, i, split) covers mask heads
+    // g*group + split*gs .. + gs - 1 of row i
     for (int32_t g = 0; g < n_g; ++g)
-      for (int32_t i = 0; i < rows; ++i) {
-        int32_t n = 0;
-        for (int32_t gh = 0; gh < group; ++gh) n += info->row_len_h[static_cast<size_t>((g * group + gh) * rows + i)];
-        for (int32_t b = 0; b < n_b; ++b) tiles.push_back({i, n, b * n_g + g});
-      }
+      for (int32_t i = 0; i < rows; ++i)
+        for (int32_t sp = 0; sp < splits; ++sp) {
+          int32_t n = 0;
+          for (int32_t gh = sp * gs; gh < (sp + 1) * gs; ++gh)
+            n += info->row_len_h[static_cast<size_t>((g * group + gh) * rows + i)];
+          for (int32_t b = 0; b < n_b; ++b) tiles.push_back({i, n, b * n_g + g, sp});
+        }
     std::stable_sort(tiles.begin(), tiles.end(), [](const T& x, const T& y) { return x.n > y.n; });
   }
   // greedy; cost in eighths of a block, with a per-tile overhead of about
@@ -61,7 +68,7 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
   for (const T& t : tiles) {
     Load top = heap.top();
     heap.pop();
-    lists[static_cast<size_t>(top.second)].push_back(make_int4(t.i, t.n, t.bg, 0));
+    lists[static_cast<size_t>(top.second)].push_back(make_int4(t.i, t.n, t.bg, t.sp));
     top.first += 8 * static_cast<int64_t>(t.n) + 12;
     heap.push(top);
   }
@@ -84,6 +91,7 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
   sc.n_b = n_b;
   sc.n_g = n_g;
   sc.group = group;
+  sc.splits = splits;
   sc.grid = grid;
   sc.device = dev;
   sc.stride = st;

@@ -151,7 +151,13 @@ typedef struct {
  * only label-1 blocks, and runs an online softmax (running max and sum, one
  * divide at the end).  `fwd_info` must be a BSA_ORIENT_FWD MaskInfo with
  * q_len == S_q, kv_len == S_kv and mask_heads 1 or Hq.  A query row with no
- * visible key gets O = 0 and LSE = -inf. */
+ * visible key gets O = 0 and LSE = -inf.  The kernel is launched with
+ * programmatic stream serialization: its set-up overlaps the end of the
+ * previous kernel on `stream`, and it waits for that kernel before reading
+ * Q/K/V or writing O/LSE (BSA_PDL=0 in the environment turns this off).
+ * The first launch of a (B, Hq, SM count) configuration builds its tile
+ * schedule (a small synchronous allocation and upload, cached in the
+ * MaskInfo). */
 BSA_API bsa_status bsa_fwd(const bsa_fwd_args* args, const bsa_mask_info* fwd_info, bsa_stream stream);
 
 typedef struct {
@@ -178,9 +184,19 @@ BSA_API bsa_status bsa_bwd(const bsa_bwd_args* args, const bsa_mask_info* fwd_in
                    bsa_stream stream);
 /* dsum[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d] (fp32). */
 BSA_API bsa_status bsa_bwd_rowsum(const bsa_bwd_args* args, bsa_stream stream);
-/* dK, dV: grid over (b, kv head, key block), queries innermost. */
+/* dK, dV: grid over (b, kv head, key block), queries innermost.  When
+ * B * Hkv * (S_kv / 128) is small next to the number of SMs (MQA, short
+ * sequences) the q heads of each group are split over several CTAs: their
+ * fp32 partial sums go to stream-ordered workspace taken from a memory pool
+ * the library keeps per device (cudaMallocFromPoolAsync, returned with
+ * cudaFreeAsync on `stream`, kept cached by the pool) and a second kernel
+ * adds them up in a fixed order.  The first launch of a configuration also
+ * builds its tile schedule (a small synchronous allocation and upload,
+ * cached in the MaskInfo); bsa_bwd_noalloc does neither. */
 BSA_API bsa_status bsa_bwd_dkv(const bsa_bwd_args* args, const bsa_mask_info* dkv_info, bsa_stream stream);
-/* dQ: grid over (b, query head, query block), keys innermost. */
+/* dQ: grid over (b, query head, query block), keys innermost.  The first
+ * launch of a configuration builds its tile schedule (cached in the MaskInfo,
+ * shared with bsa_fwd). */
 BSA_API bsa_status bsa_bwd_dq(const bsa_bwd_args* args, const bsa_mask_info* fwd_info, bsa_stream stream);
 
 /* The backward pass (rowsum, dK/dV, dQ, same arguments and results as
