@@ -443,6 +443,49 @@ def run_reference(args):
     return out
 
 
+KERNEL_SOURCES = {"fwd_kernel": "attn_fwd.cu", "rowsum_kernel": "attn_bwd_rowsum.cu", "dkv_kernel": "attn_bwd.cu",
+                  "dq_kernel": "attn_bwd.cu"}
+
+
+def ingest_ncu(report: str, workload: str):
+    """Writes profiles/traffic.json's entry for `workload` from an ncu report
+    of the bench (first launch of each attention kernel): DRAM bytes per
+    launch, tied to the sha of the kernel's source file."""
+    import csv
+    import hashlib
+    import io
+    import re
+    import subprocess
+    raw = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], capture_output=True, text=True,
+                         check=True).stdout
+    rows = list(csv.reader(io.StringIO(raw)))
+    hdr, units = rows[0], rows[1]
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+
+    def val(r, name):
+        i = hdr.index(name)
+        return float(r[i].replace(",", "")) * scale[units[i]]
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    table = json.load(open(path)) if os.path.exists(path) else {}
+    ent = {}
+    for r in rows[2:]:
+        names = re.findall(r"::(\w+)(?:<[^()]*>)?\(", r[hdr.index("Kernel Name")])
+        k = names[-1] if names else ""
+        if k not in KERNEL_SOURCES or k in ent:
+            continue
+        src = KERNEL_SOURCES[k]
+        with open(os.path.join(ROOT, "block_sparse_attention_process_gb300", "csrc", src), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        rd, wr = val(r, "dram__bytes_read.sum"), val(r, "dram__bytes_write.sum")
+        ent[k] = {"bytes_per_launch": int(rd + wr), "dram_read_mb": round(rd / 1e6, 6), "dram_write_mb": round(wr / 1e6, 6),
+                  "source": src, "source_sha": sha, "valid": True}
+    table[workload] = ent
+    with open(path, "w") as f:
+        json.dump(table, f, indent=1)
+    print(json.dumps(ent))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,7 +495,12 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ingest-ncu", metavar="REPORT",
+                    help="write profiles/traffic.json for --workload from an ncu report of this bench, then exit")
     args = ap.parse_args()
+    if args.ingest_ncu:
+        ingest_ncu(args.ingest_ncu, args.workload)
+        return
     if args.warmup < 3 and args.impl == "gb300":
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
