@@ -24,6 +24,10 @@ What it computes, and the passage each piece follows:
   Attention on a TPU, Line by Line", sections "What does the TPU flash
   attention kernel save for the backward pass?" and "Why does the TPU flash
   attention backward pass run two kernels instead of one?".
+* ``shards``     -- attention over one shard of the key axis (unnormalised
+  accumulator, maximum, normaliser) and the merge of shards with the
+  flash rescaling and one final divide (Splash page, "What does ring
+  attention add on top of the splash kernel?").
 
 Every function is pinned by ``tests/test_oracle_*.py`` against what the
 pages print (block counts, grid widths, partial-block bytes), closed forms,
