@@ -168,6 +168,40 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, info: MaskInfo, *, o:
     return o, lse
 
 
+def fwd_partial(q: torch.Tensor, k_shard: torch.Tensor, v_shard: torch.Tensor, info: MaskInfo, kv_offset: int, *,
+                softmax_scale: Optional[float] = None, stream=None):
+    """bsa_fwd_partial: attention of q over one key shard (k_shard / v_shard hold keys
+    kv_offset .. kv_offset + Skv_shard - 1 of the MaskInfo's key axis).
+    -> (o_acc fp32 [B,Hq,S,D], m fp32 [B,Hq,S], l fp32 [B,Hq,S])."""
+    for n, t in (("q", q), ("k", k_shard), ("v", v_shard)):
+        _check_bf16(n, t)
+    B, Hq, S, D = q.shape
+    Hkv, Skv = k_shard.shape[1], k_shard.shape[2]
+    o_acc = torch.empty((B, Hq, S, D), dtype=torch.float32, device=q.device)
+    m = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    l = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    a = _abi.FwdPartialArgs(_ptr(q), _ptr(k_shard), _ptr(v_shard), _ptr(o_acc), _ptr(m), _ptr(l), B, Hq, Hkv, D, S,
+                            Skv, kv_offset, math.nan if softmax_scale is None else softmax_scale)
+    check(_abi.lib().bsa_fwd_partial(C.byref(a), info.handle, _stream(stream)), "bsa_fwd_partial")
+    return o_acc, m, l
+
+
+def fwd_merge(o_acc: torch.Tensor, m: torch.Tensor, l: torch.Tensor, stream=None):
+    """bsa_fwd_merge over stacked shards: o_acc [n, B,Hq,S,D], m / l [n, B,Hq,S] fp32
+    -> (o bf16 [B,Hq,S,D], lse fp32 [B,Hq,S])."""
+    for n_, t in (("o_acc", o_acc), ("m", m), ("l", l)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n_} must be a contiguous CUDA float32 tensor")
+    n = o_acc.shape[0]
+    D = o_acc.shape[-1]
+    rows = o_acc[0].numel() // D
+    o = torch.empty(o_acc.shape[1:], dtype=torch.bfloat16, device=o_acc.device)
+    lse = torch.empty(m.shape[1:], dtype=torch.float32, device=o_acc.device)
+    a = _abi.MergeArgs(n, _ptr(o_acc), _ptr(m), _ptr(l), _ptr(o), _ptr(lse), rows, D)
+    check(_abi.lib().bsa_fwd_merge(C.byref(a), _stream(stream)), "bsa_fwd_merge")
+    return o, lse
+
+
 @dataclass
 class _BwdBufs:
     args: _abi.BwdArgs

@@ -46,6 +46,18 @@ class FwdArgs(C.Structure):
                 ("D", C.c_int32), ("S_q", C.c_int64), ("S_kv", C.c_int64), ("softmax_scale", C.c_float)]
 
 
+class FwdPartialArgs(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("o_acc", C.c_void_p),
+                ("m", C.c_void_p), ("l", C.c_void_p), ("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32),
+                ("D", C.c_int32), ("S_q", C.c_int64), ("S_kv_shard", C.c_int64), ("kv_offset", C.c_int64),
+                ("softmax_scale", C.c_float)]
+
+
+class MergeArgs(C.Structure):
+    _fields_ = [("n_shards", C.c_int32), ("o_acc", C.c_void_p), ("m", C.c_void_p), ("l", C.c_void_p),
+                ("o", C.c_void_p), ("lse", C.c_void_p), ("rows", C.c_int64), ("D", C.c_int32)]
+
+
 class BwdArgs(C.Structure):
     _fields_ = [("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("o", C.c_void_p),
                 ("lse", C.c_void_p), ("do_", C.c_void_p), ("dq", C.c_void_p), ("dk", C.c_void_p),
@@ -60,6 +72,8 @@ SIGNATURES = {
     "bsa_mask_info_view": (C.c_int, [C.c_void_p, C.POINTER(MaskInfoDesc)]),
     "bsa_mask_info_destroy": (C.c_int, [C.c_void_p]),
     "bsa_fwd": (C.c_int, [C.POINTER(FwdArgs), C.c_void_p, C.c_void_p]),
+    "bsa_fwd_partial": (C.c_int, [C.POINTER(FwdPartialArgs), C.c_void_p, C.c_void_p]),
+    "bsa_fwd_merge": (C.c_int, [C.POINTER(MergeArgs), C.c_void_p]),
     "bsa_bwd": (C.c_int, [C.POINTER(BwdArgs), C.c_void_p, C.c_void_p, C.c_void_p]),
     "bsa_bwd_rowsum": (C.c_int, [C.POINTER(BwdArgs), C.c_void_p]),
     "bsa_bwd_noalloc": (C.c_int, [C.POINTER(BwdArgs), C.c_void_p, C.c_void_p, C.c_void_p]),

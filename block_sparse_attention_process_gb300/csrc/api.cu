@@ -306,6 +306,38 @@ bsa_status bsa_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, bsa_stream 
   return fwd_launch(a, info, resolve_scale(a->softmax_scale, a->D), static_cast<cudaStream_t>(stream));
 }
 
+bsa_status bsa_fwd_partial(const bsa_fwd_partial_args* a, const bsa_mask_info* info, bsa_stream stream) {
+  if (!a) return fail(BSA_ERR_INVALID_ARG, "args is null");
+  bsa_status s = check_shapes(a->B, a->Hq, a->Hkv, a->S_q, a->S_kv_shard, a->D);
+  if (s != BSA_OK) return s;
+  if (!a->q || !a->k || !a->v || !a->o_acc || !a->m || !a->l)
+    return fail(BSA_ERR_INVALID_ARG, "a tensor pointer is null");
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o_acc) || !aligned16(a->m) ||
+      !aligned16(a->l))
+    return fail(BSA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!info) return fail(BSA_ERR_INVALID_ARG, "forward MaskInfo is null");
+  if (a->kv_offset < 0 || a->kv_offset % kBlock)
+    return fail(BSA_ERR_INVALID_ARG, "kv_offset must be a non-negative multiple of 128");
+  if (a->kv_offset + a->S_kv_shard > info->kv_len)
+    return fail(BSA_ERR_INVALID_ARG, "the shard runs past the MaskInfo's key axis");
+  s = check_info(info, BSA_ORIENT_FWD, a->S_q, info->kv_len, a->Hq, "forward");
+  if (s != BSA_OK) return s;
+  return fwd_partial_launch(a, info, resolve_scale(a->softmax_scale, a->D), static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_fwd_merge(const bsa_merge_args* a, bsa_stream stream) {
+  if (!a) return fail(BSA_ERR_INVALID_ARG, "args is null");
+  if (a->n_shards < 1) return fail(BSA_ERR_INVALID_ARG, "n_shards must be at least 1");
+  if (a->rows <= 0) return fail(BSA_ERR_INVALID_ARG, "rows must be positive");
+  if (a->D != 64 && a->D != 128) return fail(BSA_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+  if (static_cast<int64_t>(a->n_shards) * a->rows * a->D > (int64_t(1) << 40))
+    return fail(BSA_ERR_UNSUPPORTED, "merge too large");
+  if (!a->o_acc || !a->m || !a->l || !a->o || !a->lse) return fail(BSA_ERR_INVALID_ARG, "a tensor pointer is null");
+  if (!aligned16(a->o_acc) || !aligned16(a->o))
+    return fail(BSA_ERR_INVALID_ARG, "o_acc and o must be 16-byte aligned");
+  return merge_launch(a, static_cast<cudaStream_t>(stream));
+}
+
 bsa_status bsa_bwd_rowsum(const bsa_bwd_args* a, bsa_stream stream) {
   bsa_status s = check_bwd(a);
   if (s != BSA_OK) return s;

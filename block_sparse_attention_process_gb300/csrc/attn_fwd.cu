@@ -102,6 +102,15 @@ struct FwdParams {
   int32_t n_tiles;
   const int4* sched;     // this launch's tile lists, sched_stride entries per CTA
   int32_t sched_stride;
+  // Key shard: only MaskInfo blocks with column in [kv_lo, kv_hi) are
+  // visited, K/V row of column c = (c - kv_lo) * 128.  With `partial` the
+  // epilogue writes the unnormalised accumulator, reference maximum
+  // (natural-log units) and normaliser instead of O and LSE.
+  int32_t kv_lo, kv_hi;
+  int32_t partial;
+  float* o_acc;
+  float* m_out;
+  float* l_out;
   uint32_t* err;
   uint64_t wait_ns;
 };
@@ -199,34 +208,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t t_hm = p.mi.heads == 1 ? 0 : t_hq;
       const int64_t t_row_base = (static_cast<int64_t>(t_hm) * p.mi.rows + t_i) * p.mi.width;
       const int64_t out_row = static_cast<int64_t>(te.z) * p.Sq + static_cast<int64_t>(t_i) * 128;
-      if (t_n == 0) {
-        // every key masked for the whole query block: O = 0, LSE = -inf
+      // blocks of this launch's key range: the whole row, or (a key shard)
+      // those found by a first pass over the row
+      const bool ranged = p.kv_lo > 0 || p.kv_hi < p.mi.cols;
+      int32_t n_in = t_n;
+      if (ranged && t_n > 0) {
+        n_in = 0;
+        int32_t j = 0;
+        for (int32_t pos = 0; pos < p.mi.width && j < t_n; ++pos) {
+          const BlockRef br = read_block(p.mi, t_row_base, pos, lane == 0 ? p.err : nullptr);
+          if (br.label == 0) continue;
+          ++j;
+          if (br.col >= p.kv_lo && br.col < p.kv_hi) ++n_in;
+        }
+      }
+      if (n_in == 0) {
+        // every key of the range masked for the whole query block:
+        // O = 0, LSE = -inf (a shard: accumulator 0, maximum -inf, normaliser 0)
         griddep_wait();
-        uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
-        for (int v = lane; v < 128 * D / 8; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-        for (int r = lane; r < 128; r += 32) p.lse[out_row + r] = -INFINITY;
+        if (p.partial) {
+          float4* dst = reinterpret_cast<float4*>(p.o_acc + out_row * D);
+          for (int v = lane; v < 128 * D / 4; v += 32) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int r = lane; r < 128; r += 32) {
+            p.m_out[out_row + r] = -INFINITY;
+            p.l_out[out_row + r] = 0.f;
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
+          for (int v = lane; v < 128 * D / 8; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+          for (int r = lane; r < 128; r += 32) p.lse[out_row + r] = -INFINITY;
+        }
         continue;
       }
       const uint32_t q0 = static_cast<uint32_t>(p.mi.q_sequence[t_i * 128]);
       const int64_t kv_base = (static_cast<int64_t>(t_b) * p.Hkv + t_hq / (p.Hq / p.Hkv)) * p.Skv;
-      int32_t j = 0;
+      int32_t j = 0, pub = 0;
       RawRef ahead = load_block(p.mi, t_row_base, 0);
       for (int32_t pos = 0; ok && pos < p.mi.width && j < t_n; ++pos) {
         const RawRef cur = ahead;
         if (pos + 1 < p.mi.width) ahead = load_block(p.mi, t_row_base, pos + 1);
         const BlockRef br = check_block(p.mi, cur, lane == 0 ? p.err : nullptr);
         if (br.label == 0) continue;
-        const uint32_t x = static_cast<uint32_t>(br.col) | (static_cast<uint32_t>(br.label) << 16) |
-                           (j == 0 ? kFirst : 0u) | (j + 1 == t_n ? kLast : 0u);
-        ok = publish(x, static_cast<uint32_t>(br.slot), q0, static_cast<uint32_t>(out_row),
-                     static_cast<uint32_t>(kv_base + static_cast<int64_t>(br.col) * 128));
         ++j;
+        if (br.col < p.kv_lo || br.col >= p.kv_hi) continue;
+        const uint32_t x = static_cast<uint32_t>(br.col) | (static_cast<uint32_t>(br.label) << 16) |
+                           (pub == 0 ? kFirst : 0u) | (pub + 1 == n_in ? kLast : 0u);
+        ok = publish(x, static_cast<uint32_t>(br.slot), q0, static_cast<uint32_t>(out_row),
+                     static_cast<uint32_t>(kv_base + static_cast<int64_t>(br.col - p.kv_lo) * 128));
+        ++pub;
       }
-      // a malformed row with fewer non-empty entries than row_len: flagged
+      // a malformed row with fewer non-empty entries than expected: flagged
       // dummy blocks keep every role's count in step
-      for (; ok && j < t_n; ++j) {
+      for (; ok && pub < n_in; ++pub) {
         if (lane == 0 && p.err) atomicOr(p.err, DEV_ERR_BOUNDS);
-        ok = publish((2u << 16) | (j == 0 ? kFirst : 0u) | (j + 1 == t_n ? kLast : 0u), 0u, q0,
+        ok = publish((2u << 16) | (pub == 0 ? kFirst : 0u) | (pub + 1 == n_in ? kLast : 0u), 0u, q0,
                      static_cast<uint32_t>(out_row), static_cast<uint32_t>(kv_base));
       }
     }
@@ -412,11 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
       const int64_t orow = static_cast<int64_t>(row0) + r;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
-      // chunks of 32 columns, the next one in flight while this one is
-      // scaled and stored (straight-line code up to each wait)
-      uint32_t va[32], vb[32];
-      auto emit = [&](const uint32_t* v, int c) {
+      // O / l in bf16, or (a key shard) the unnormalised fp32 accumulator
+      auto emit_bf16 = [&](const uint32_t* v, int c) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           uint4 o4;
@@ -427,28 +460,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[c * 4 + e] = o4;
         }
       };
-      tmem_ld32(obase, va);
-      tmem_wait_ld();
-      reg_fence32(va);
+      auto emit_acc = [&](const uint32_t* v, int c) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o_acc + orow * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; c += 2) {
-        if (c + 1 < D / 32) tmem_ld32(obase + (c + 1) * 32, vb);
-        emit(va, c);
-        if (c + 1 < D / 32) {
-          tmem_wait_ld();
-          reg_fence32(vb);
-          if (c + 2 < D / 32) tmem_ld32(obase + (c + 2) * 32, va);
-          emit(vb, c + 1);
-          if (c + 2 < D / 32) {
+        for (int e = 0; e < 8; ++e) dst[c * 8 + e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+      };
+      // chunks of 32 columns, the next one in flight while this one is
+      // stored (straight-line code up to each wait)
+      auto drain = [&](auto emit) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(obase, va);
+        tmem_wait_ld();
+        reg_fence32(va);
+#pragma unroll
+        for (int c = 0; c < D / 32; c += 2) {
+          if (c + 1 < D / 32) tmem_ld32(obase + (c + 1) * 32, vb);
+          emit(va, c);
+          if (c + 1 < D / 32) {
             tmem_wait_ld();
-            reg_fence32(va);
+            reg_fence32(vb);
+            if (c + 2 < D / 32) tmem_ld32(obase + (c + 2) * 32, va);
+            emit(vb, c + 1);
+            if (c + 2 < D / 32) {
+              tmem_wait_ld();
+              reg_fence32(va);
+            }
           }
         }
-      }
+      };
+      if (p.partial) drain(emit_acc);
+      else drain(emit_bf16);
       // (every load of this tile's O has completed by the last wait)
       tc_fence_before();
       mbar_arrive(&s.o_empty);
-      p.lse[orow] = l_row > 0.f ? (mrow + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+      if (p.partial) {
+        p.m_out[orow] = l_row > 0.f ? mrow * 0.69314718055994530942f : -INFINITY;
+        p.l_out[orow] = l_row;
+      } else {
+        p.lse[orow] = l_row > 0.f ? (mrow + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+      }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax (kParts warpgroups)
@@ -647,28 +697,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// One forward launch: the whole key axis (O, LSE) or one key shard
+// (accumulator, maximum, normaliser).
+struct FwdCall {
+  const void *q, *k, *v;
+  int32_t B, Hq, Hkv;
+  int64_t Sq, Skv;  // Skv: keys in k / v (the shard's length for a shard)
+  __nv_bfloat16* o;
+  float* lse;
+  float *o_acc, *m, *l;
+  int32_t kv_lo, kv_hi, partial;
+};
+
 template <int D>
-bsa_status launch_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream) {
+bsa_status launch_fwd(const FwdCall& c, const bsa_mask_info* info, float scale, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
-  const uint64_t q_rows = static_cast<uint64_t>(a->B) * a->Hq * a->S_q;
-  const uint64_t kv_rows = static_cast<uint64_t>(a->B) * a->Hkv * a->S_kv;
-  if (!make_tmap_bf16_2d(&tq, a->q, q_rows, D, D * 2, 128, 64) ||
-      !make_tmap_bf16_2d(&tk, a->k, kv_rows, D, D * 2, 128, 64) ||
-      !make_tmap_bf16_2d(&tv, a->v, kv_rows, D, D * 2, 128, 64))
+  const uint64_t q_rows = static_cast<uint64_t>(c.B) * c.Hq * c.Sq;
+  const uint64_t kv_rows = static_cast<uint64_t>(c.B) * c.Hkv * c.Skv;
+  if (!make_tmap_bf16_2d(&tq, c.q, q_rows, D, D * 2, 128, 64) ||
+      !make_tmap_bf16_2d(&tk, c.k, kv_rows, D, D * 2, 128, 64) ||
+      !make_tmap_bf16_2d(&tv, c.v, kv_rows, D, D * 2, 128, 64))
     return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a Q/K/V description");
   FwdParams p{};
-  p.B = a->B;
-  p.Hq = a->Hq;
-  p.Hkv = a->Hkv;
-  p.Sq = a->S_q;
-  p.Skv = a->S_kv;
-  p.nQ = static_cast<int32_t>(a->S_q / 128);
-  p.nK = static_cast<int32_t>(a->S_kv / 128);
+  p.B = c.B;
+  p.Hq = c.Hq;
+  p.Hkv = c.Hkv;
+  p.Sq = c.Sq;
+  p.Skv = c.Skv;
+  p.nQ = static_cast<int32_t>(c.Sq / 128);
+  p.nK = static_cast<int32_t>(c.Skv / 128);
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.o = static_cast<__nv_bfloat16*>(a->o);
-  p.lse = a->lse;
+  p.o = c.o;
+  p.lse = c.lse;
+  p.o_acc = c.o_acc;
+  p.m_out = c.m;
+  p.l_out = c.l;
+  p.kv_lo = c.kv_lo;
+  p.kv_hi = c.kv_hi;
+  p.partial = c.partial;
   p.mi = mask_info_dev(info);
-  p.n_tiles = a->B * a->Hq * p.nQ;
+  p.n_tiles = c.B * c.Hq * p.nQ;
   p.err = device_error_word();
   p.wait_ns = wait_limit_ns();
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
@@ -680,7 +748,7 @@ bsa_status launch_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, float sc
     attr_set = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  bsa_status st = tile_schedule(info, a->B, a->Hq, 1, 1, grid, &p.sched, &p.sched_stride);
+  bsa_status st = tile_schedule(info, c.B, c.Hq, 1, 1, grid, &p.sched, &p.sched_stride);
   if (st != BSA_OK) return st;
   cudaError_t e = launch_kernel(fwd_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -688,11 +756,49 @@ bsa_status launch_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, float sc
   return BSA_OK;
 }
 
+bsa_status dispatch(const FwdCall& c, int D, const bsa_mask_info* info, float scale, cudaStream_t stream) {
+  if (D == 128) return launch_fwd<128>(c, info, scale, stream);
+  return launch_fwd<64>(c, info, scale, stream);
+}
+
 }  // namespace
 
 bsa_status fwd_launch(const bsa_fwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream) {
-  if (a->D == 128) return launch_fwd<128>(a, info, scale, stream);
-  return launch_fwd<64>(a, info, scale, stream);
+  FwdCall c{};
+  c.q = a->q;
+  c.k = a->k;
+  c.v = a->v;
+  c.B = a->B;
+  c.Hq = a->Hq;
+  c.Hkv = a->Hkv;
+  c.Sq = a->S_q;
+  c.Skv = a->S_kv;
+  c.o = static_cast<__nv_bfloat16*>(a->o);
+  c.lse = a->lse;
+  c.kv_lo = 0;
+  c.kv_hi = info->cols;
+  c.partial = 0;
+  return dispatch(c, a->D, info, scale, stream);
+}
+
+bsa_status fwd_partial_launch(const bsa_fwd_partial_args* a, const bsa_mask_info* info, float scale,
+                              cudaStream_t stream) {
+  FwdCall c{};
+  c.q = a->q;
+  c.k = a->k;
+  c.v = a->v;
+  c.B = a->B;
+  c.Hq = a->Hq;
+  c.Hkv = a->Hkv;
+  c.Sq = a->S_q;
+  c.Skv = a->S_kv_shard;
+  c.o_acc = a->o_acc;
+  c.m = a->m;
+  c.l = a->l;
+  c.kv_lo = static_cast<int32_t>(a->kv_offset / 128);
+  c.kv_hi = static_cast<int32_t>((a->kv_offset + a->S_kv_shard) / 128);
+  c.partial = 1;
+  return dispatch(c, a->D, info, scale, stream);
 }
 
 }  // namespace bsa

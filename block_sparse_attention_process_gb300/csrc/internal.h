@@ -50,6 +50,9 @@ uint64_t wait_limit_ns();
 bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opts, cudaStream_t stream,
                              bsa_mask_info** out);
 bsa_status fwd_launch(const bsa_fwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream);
+bsa_status fwd_partial_launch(const bsa_fwd_partial_args* a, const bsa_mask_info* info, float scale,
+                              cudaStream_t stream);
+bsa_status merge_launch(const bsa_merge_args* a, cudaStream_t stream);
 bsa_status rowsum_launch(const bsa_bwd_args* a, cudaStream_t stream);
 // `err` (optional) replaces the library's device error word for this launch;
 // `schedule` false hands tiles out round-robin instead of building (and

@@ -160,6 +160,55 @@ typedef struct {
  * MaskInfo). */
 BSA_API bsa_status bsa_fwd(const bsa_fwd_args* args, const bsa_mask_info* fwd_info, bsa_stream stream);
 
+/* One shard of the key axis ("Splash Attention: When the Mask Stops Being
+ * Arithmetic and Becomes the Loop", "What does ring attention add on top of
+ * the splash kernel?"): the keys and values are split into shards, each
+ * shard's attention runs with the MaskInfo cut to the shard's key range,
+ * and the per-shard results are merged with the flash rescaling
+ * (bsa_fwd_merge).  The shard's K and V are given on their own; the
+ * MaskInfo is the one for the whole key axis. */
+typedef struct {
+  const void* q;        /* bf16 [B, Hq, S_q, D] */
+  const void* k;        /* bf16 [B, Hkv, S_kv_shard, D]: keys kv_offset .. kv_offset + S_kv_shard - 1 */
+  const void* v;        /* bf16 [B, Hkv, S_kv_shard, D] */
+  float* o_acc;         /* fp32 [B, Hq, S_q, D], written: sum over the shard's visible keys of
+                           exp(s - m) v (0 for a row with no visible key in the shard) */
+  float* m;             /* fp32 [B, Hq, S_q], written: the row's reference maximum of the scaled
+                           scores, natural-log units (-inf for a row with no visible key); it may
+                           lag the true maximum by up to 8 log2 units: only m + log(l) and
+                           o_acc / l are determined */
+  float* l;             /* fp32 [B, Hq, S_q], written: sum over the shard's visible keys of exp(s - m) */
+  int32_t B, Hq, Hkv, D;
+  int64_t S_q;
+  int64_t S_kv_shard;   /* multiple of 128 */
+  int64_t kv_offset;    /* the shard's first key on the MaskInfo's key axis, multiple of 128 */
+  float softmax_scale;  /* NaN selects 1/sqrt(D) */
+} bsa_fwd_partial_args;
+
+/* Forward over one key shard: the same kernel as bsa_fwd, walking only the
+ * MaskInfo blocks whose key block lies in [kv_offset, kv_offset + S_kv_shard)
+ * and writing the unnormalised accumulator, maximum and normaliser instead
+ * of O and LSE.  Requires kv_offset + S_kv_shard <= the MaskInfo's kv_len. */
+BSA_API bsa_status bsa_fwd_partial(const bsa_fwd_partial_args* args, const bsa_mask_info* fwd_info,
+                                   bsa_stream stream);
+
+typedef struct {
+  int32_t n_shards;     /* >= 1 */
+  const float* o_acc;   /* fp32 [n_shards, rows, D]: the shards' o_acc, one after the other */
+  const float* m;       /* fp32 [n_shards, rows] */
+  const float* l;       /* fp32 [n_shards, rows] */
+  void* o;              /* bf16 [rows, D], written: sum_i exp(m_i - M) o_acc_i / L */
+  float* lse;           /* fp32 [rows], written: M + log L (-inf when every shard is empty) */
+  int64_t rows;         /* B * Hq * S_q */
+  int32_t D;
+} bsa_merge_args;
+
+/* Merge of key shards (same section): M = max of the shards' m over shards
+ * with l > 0, L = sum_i exp(m_i - M) l_i, one final divide.  A shard that is
+ * empty for a row (l = 0) contributes nothing; a row empty in every shard
+ * gets O = 0 and LSE = -inf. */
+BSA_API bsa_status bsa_fwd_merge(const bsa_merge_args* args, bsa_stream stream);
+
 typedef struct {
   const void* q, *k, *v; /* as in bsa_fwd_args */
   const void* o;         /* bf16 forward output */

@@ -131,3 +131,52 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _abi.lib()
+
+
+def _partial_args(**kw):
+    from block_sparse_attention_process_gb300 import _abi
+    a = _abi.FwdPartialArgs(16, 32, 48, 64, 80, 96, 1, 2, 2, 128, 256, 128, 128, math.nan)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"S_kv_shard": 100}, "INVALID_ARG"),
+    ({"kv_offset": 64}, "INVALID_ARG"),
+    ({"kv_offset": -128}, "INVALID_ARG"),
+    ({"D": 96}, "UNSUPPORTED"),
+    ({"o_acc": None}, "INVALID_ARG"),
+    ({"m": 8}, "INVALID_ARG"),  # misaligned
+])
+def test_fwd_partial_rejects_bad_arguments_on_host(kw, status):
+    ensure_built()
+    from block_sparse_attention_process_gb300 import _abi
+    L = _abi.lib()
+    a = _partial_args(**kw)
+    st = L.bsa_fwd_partial(C.byref(a), C.c_void_p(1), None)
+    assert st == getattr(_abi, status), L.bsa_last_error()
+
+
+def test_fwd_partial_rejects_null_maskinfo():
+    ensure_built()
+    from block_sparse_attention_process_gb300 import _abi
+    L = _abi.lib()
+    assert L.bsa_fwd_partial(C.byref(_partial_args()), None, None) == _abi.INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"n_shards": 0}, "INVALID_ARG"),
+    ({"rows": 0}, "INVALID_ARG"),
+    ({"D": 96}, "UNSUPPORTED"),
+    ({"lse": None}, "INVALID_ARG"),
+    ({"o_acc": 8}, "INVALID_ARG"),  # misaligned
+])
+def test_fwd_merge_rejects_bad_arguments_on_host(kw, status):
+    ensure_built()
+    from block_sparse_attention_process_gb300 import _abi
+    L = _abi.lib()
+    a = _abi.MergeArgs(2, 16, 32, 48, 64, 80, 256, 128)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    assert L.bsa_fwd_merge(C.byref(a), None) == getattr(_abi, status), L.bsa_last_error()
