@@ -24,6 +24,9 @@ What it computes, and the passage each piece follows:
   Attention on a TPU, Line by Line", sections "What does the TPU flash
   attention kernel save for the backward pass?" and "Why does the TPU flash
   attention backward pass run two kernels instead of one?".
+  Optional soft cap and attention sinks follow the ``logits_soft_cap`` and
+  ``softmax_aux`` arguments of the EasyDeL ``blocksparse_attention``
+  operator page.
 * ``shards``     -- attention over one shard of the key axis (unnormalised
   accumulator, maximum, normaliser) and the merge of shards with the
   flash rescaling and one final divide (Splash page, "What does ring

@@ -168,7 +168,7 @@ def test_full_size_sampled_heads(name, heads):
         rdk = np.zeros(k.shape[2:])
         rdv = np.zeros(v.shape[2:])
         for h in range(g * group, (g + 1) * group):
-            rdq, dkh, dvh, _, _, _ = oatt.head_backward(f64(q[b, h]), f64(k[b, g]), f64(v[b, g]), f64(do[b, h]),
+            rdq, dkh, dvh, _, _, _, _ = oatt.head_backward(f64(q[b, h]), f64(k[b, g]), f64(v[b, g]), f64(do[b, h]),
                                                         oatt.mask_rows_for(mask, 0), scale)
             rdk += dkh
             rdv += dvh
