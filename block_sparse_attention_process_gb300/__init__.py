@@ -151,9 +151,26 @@ def _check_bf16(name: str, t: torch.Tensor) -> None:
         raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
 
 
+def _sink_fields(sinks: Optional[torch.Tensor], Hkv: int):
+    """(pointer, count, per-kv-head flag) of an fp32 CUDA sinks tensor [Hkv, n] or [n]."""
+    if sinks is None:
+        return None, 0, 0
+    if sinks.dtype != torch.float32 or not sinks.is_cuda or not sinks.is_contiguous():
+        raise ValueError("sinks must be a contiguous CUDA float32 tensor")
+    if sinks.dim() == 2:
+        if sinks.shape[0] != Hkv:
+            raise ValueError("a 2-D sinks tensor must be [Hkv, num_sinks]")
+        return _ptr(sinks), sinks.shape[1], 1
+    if sinks.dim() != 1:
+        raise ValueError("sinks must be [Hkv, num_sinks] or [num_sinks]")
+    return _ptr(sinks), sinks.shape[0], 0
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, info: MaskInfo, *, o: Optional[torch.Tensor] = None,
-        lse: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None, stream=None):
-    """bsa_fwd.  q [B,Hq,S,D], k/v [B,Hkv,Skv,D] bf16 -> (o bf16 [B,Hq,S,D], lse fp32 [B,Hq,S])."""
+        lse: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
+        logits_soft_cap: Optional[float] = None, sinks: Optional[torch.Tensor] = None, stream=None):
+    """bsa_fwd.  q [B,Hq,S,D], k/v [B,Hkv,Skv,D] bf16 -> (o bf16 [B,Hq,S,D], lse fp32 [B,Hq,S]).
+    Optional soft cap c (scores -> c*tanh(s/c)) and sinks (fp32 [Hkv, n] or [n])."""
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n, t)
     B, Hq, S, D = q.shape
@@ -162,14 +179,15 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, info: MaskInfo, *, o:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    sp, sn, skv = _sink_fields(sinks, Hkv)
     a = _abi.FwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, D, S, Skv,
-                     math.nan if softmax_scale is None else softmax_scale)
+                     math.nan if softmax_scale is None else softmax_scale, logits_soft_cap or 0.0, sp, sn, skv)
     check(_abi.lib().bsa_fwd(C.byref(a), info.handle, _stream(stream)), "bsa_fwd")
     return o, lse
 
 
 def fwd_partial(q: torch.Tensor, k_shard: torch.Tensor, v_shard: torch.Tensor, info: MaskInfo, kv_offset: int, *,
-                softmax_scale: Optional[float] = None, stream=None):
+                softmax_scale: Optional[float] = None, logits_soft_cap: Optional[float] = None, stream=None):
     """bsa_fwd_partial: attention of q over one key shard (k_shard / v_shard hold keys
     kv_offset .. kv_offset + Skv_shard - 1 of the MaskInfo's key axis).
     -> (o_acc fp32 [B,Hq,S,D], m fp32 [B,Hq,S], l fp32 [B,Hq,S])."""
@@ -181,7 +199,8 @@ def fwd_partial(q: torch.Tensor, k_shard: torch.Tensor, v_shard: torch.Tensor, i
     m = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     l = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     a = _abi.FwdPartialArgs(_ptr(q), _ptr(k_shard), _ptr(v_shard), _ptr(o_acc), _ptr(m), _ptr(l), B, Hq, Hkv, D, S,
-                            Skv, kv_offset, math.nan if softmax_scale is None else softmax_scale)
+                            Skv, kv_offset, math.nan if softmax_scale is None else softmax_scale,
+                            logits_soft_cap or 0.0)
     check(_abi.lib().bsa_fwd_partial(C.byref(a), info.handle, _stream(stream)), "bsa_fwd_partial")
     return o_acc, m, l
 
@@ -209,9 +228,11 @@ class _BwdBufs:
     dk: torch.Tensor
     dv: torch.Tensor
     dsum: torch.Tensor
+    dsinks: Optional[torch.Tensor] = None
 
 
-def _bwd_args(q, k, v, o, lse, do, dq, dk, dv, dsum, softmax_scale, grad_fp32) -> _BwdBufs:
+def _bwd_args(q, k, v, o, lse, do, dq, dk, dv, dsum, softmax_scale, grad_fp32, logits_soft_cap=None,
+              sinks=None) -> _BwdBufs:
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check_bf16(n, t)
     B, Hq, S, D = q.shape
@@ -221,18 +242,20 @@ def _bwd_args(q, k, v, o, lse, do, dq, dk, dv, dsum, softmax_scale, grad_fp32) -
     dk = torch.empty(k.shape, dtype=gdt, device=q.device) if dk is None else dk
     dv = torch.empty(v.shape, dtype=gdt, device=q.device) if dv is None else dv
     dsum = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if dsum is None else dsum
+    sp, sn, skv = _sink_fields(sinks, Hkv)
+    dsinks = None if sinks is None else torch.empty_like(sinks)
     a = _abi.BwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
                      _ptr(dsum), B, Hq, Hkv, D, S, Skv, math.nan if softmax_scale is None else softmax_scale,
-                     1 if grad_fp32 else 0)
-    return _BwdBufs(a, dq, dk, dv, dsum)
+                     1 if grad_fp32 else 0, logits_soft_cap or 0.0, sp, _ptr(dsinks), sn, skv)
+    return _BwdBufs(a, dq, dk, dv, dsum, dsinks)
 
 
 def bwd(q, k, v, o, lse, do, fwd_info: MaskInfo, dkv_info: MaskInfo, *, dq=None, dk=None, dv=None, dsum=None,
-        softmax_scale=None, grad_fp32: bool = False, stream=None):
-    """bsa_bwd: rowsum, then dK/dV, then dQ.  Returns (dq, dk, dv)."""
-    b = _bwd_args(q, k, v, o, lse, do, dq, dk, dv, dsum, softmax_scale, grad_fp32)
+        softmax_scale=None, grad_fp32: bool = False, logits_soft_cap=None, sinks=None, stream=None):
+    """bsa_bwd: rowsum, then dK/dV, then dQ.  Returns (dq, dk, dv), plus dsinks when sinks are given."""
+    b = _bwd_args(q, k, v, o, lse, do, dq, dk, dv, dsum, softmax_scale, grad_fp32, logits_soft_cap, sinks)
     check(_abi.lib().bsa_bwd(C.byref(b.args), fwd_info.handle, dkv_info.handle, _stream(stream)), "bsa_bwd")
-    return b.dq, b.dk, b.dv
+    return (b.dq, b.dk, b.dv) if sinks is None else (b.dq, b.dk, b.dv, b.dsinks)
 
 
 def bwd_noalloc(q, k, v, o, lse, do, fwd_info: MaskInfo, dkv_info: MaskInfo, *, dq, dk, dv, softmax_scale=None,

@@ -43,14 +43,16 @@ class MaskInfoDesc(C.Structure):
 class FwdArgs(C.Structure):
     _fields_ = [("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("o", C.c_void_p),
                 ("lse", C.c_void_p), ("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32),
-                ("D", C.c_int32), ("S_q", C.c_int64), ("S_kv", C.c_int64), ("softmax_scale", C.c_float)]
+                ("D", C.c_int32), ("S_q", C.c_int64), ("S_kv", C.c_int64), ("softmax_scale", C.c_float),
+                ("logits_soft_cap", C.c_float), ("sinks", C.c_void_p), ("num_sinks", C.c_int32),
+                ("sinks_per_kv_head", C.c_int32)]
 
 
 class FwdPartialArgs(C.Structure):
     _fields_ = [("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p), ("o_acc", C.c_void_p),
                 ("m", C.c_void_p), ("l", C.c_void_p), ("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32),
                 ("D", C.c_int32), ("S_q", C.c_int64), ("S_kv_shard", C.c_int64), ("kv_offset", C.c_int64),
-                ("softmax_scale", C.c_float)]
+                ("softmax_scale", C.c_float), ("logits_soft_cap", C.c_float)]
 
 
 class MergeArgs(C.Structure):
@@ -63,7 +65,9 @@ class BwdArgs(C.Structure):
                 ("lse", C.c_void_p), ("do_", C.c_void_p), ("dq", C.c_void_p), ("dk", C.c_void_p),
                 ("dv", C.c_void_p), ("dsum", C.c_void_p), ("B", C.c_int32), ("Hq", C.c_int32),
                 ("Hkv", C.c_int32), ("D", C.c_int32), ("S_q", C.c_int64), ("S_kv", C.c_int64),
-                ("softmax_scale", C.c_float), ("grad_fp32", C.c_int32)]
+                ("softmax_scale", C.c_float), ("grad_fp32", C.c_int32), ("logits_soft_cap", C.c_float),
+                ("sinks", C.c_void_p), ("dsinks", C.c_void_p), ("num_sinks", C.c_int32),
+                ("sinks_per_kv_head", C.c_int32)]
 
 
 # name -> (restype, argtypes); every symbol include/bsa.h declares

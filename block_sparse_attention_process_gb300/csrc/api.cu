@@ -159,6 +159,15 @@ bsa_status check_info(const bsa_mask_info* info, int32_t orientation, int64_t Sq
 
 float resolve_scale(float s, int32_t D) { return std::isnan(s) ? 1.0f / std::sqrt((float)D) : s; }
 
+bsa_status check_transforms(float cap, const float* sinks, int32_t num_sinks) {
+  if (!(cap >= 0.f) || std::isinf(cap)) return fail(BSA_ERR_INVALID_ARG, "logits_soft_cap must be finite and >= 0");
+  if (num_sinks < 0 || num_sinks > 64) return fail(BSA_ERR_UNSUPPORTED, "num_sinks must be in 0..64");
+  if (num_sinks > 0 && !sinks) return fail(BSA_ERR_INVALID_ARG, "sinks is null");
+  if (num_sinks > 0 && (reinterpret_cast<uintptr_t>(sinks) & 3u))
+    return fail(BSA_ERR_INVALID_ARG, "sinks must be 4-byte aligned");
+  return BSA_OK;
+}
+
 bsa_status check_bwd(const bsa_bwd_args* a) {
   if (!a) return fail(BSA_ERR_INVALID_ARG, "args is null");
   bsa_status s = check_shapes(a->B, a->Hq, a->Hkv, a->S_q, a->S_kv, a->D);
@@ -168,6 +177,10 @@ bsa_status check_bwd(const bsa_bwd_args* a) {
     if (!p) return fail(BSA_ERR_INVALID_ARG, "a tensor pointer is null");
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(BSA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  s = check_transforms(a->logits_soft_cap, a->sinks, a->num_sinks);
+  if (s != BSA_OK) return s;
+  if (a->dsinks && (reinterpret_cast<uintptr_t>(a->dsinks) & 3u))
+    return fail(BSA_ERR_INVALID_ARG, "dsinks must be 4-byte aligned");
   return BSA_OK;
 }
 
@@ -301,6 +314,8 @@ bsa_status bsa_fwd(const bsa_fwd_args* a, const bsa_mask_info* info, bsa_stream 
   if (!a->q || !a->k || !a->v || !a->o || !a->lse) return fail(BSA_ERR_INVALID_ARG, "a tensor pointer is null");
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o) || !aligned16(a->lse))
     return fail(BSA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  s = check_transforms(a->logits_soft_cap, a->sinks, a->num_sinks);
+  if (s != BSA_OK) return s;
   s = check_info(info, BSA_ORIENT_FWD, a->S_q, a->S_kv, a->Hq, "forward");
   if (s != BSA_OK) return s;
   return fwd_launch(a, info, resolve_scale(a->softmax_scale, a->D), static_cast<cudaStream_t>(stream));
@@ -318,6 +333,8 @@ bsa_status bsa_fwd_partial(const bsa_fwd_partial_args* a, const bsa_mask_info* i
   if (!info) return fail(BSA_ERR_INVALID_ARG, "forward MaskInfo is null");
   if (a->kv_offset < 0 || a->kv_offset % kBlock)
     return fail(BSA_ERR_INVALID_ARG, "kv_offset must be a non-negative multiple of 128");
+  s = check_transforms(a->logits_soft_cap, nullptr, 0);
+  if (s != BSA_OK) return s;
   if (a->kv_offset + a->S_kv_shard > info->kv_len)
     return fail(BSA_ERR_INVALID_ARG, "the shard runs past the MaskInfo's key axis");
   s = check_info(info, BSA_ORIENT_FWD, a->S_q, info->kv_len, a->Hq, "forward");

@@ -65,6 +65,10 @@ struct BwdParams {
   int32_t B, Hq, Hkv, nQ, nK;
   int64_t Sq, Skv;
   float scale, scale_log2;
+  // soft cap c (off when cap_scale == 0): scaled score -> c*tanh(s/c), in
+  // log2 units cap_log2 * tanh(raw * cap_scale) with cap_scale = scale / c;
+  // dS then also carries the factor 1 - tanh^2
+  float cap_log2, cap_scale;
   const float* lse;
   const float* dsum;
   void* dq;
@@ -296,7 +300,8 @@ struct DqSeq {
   }
 };
 
-template <int D>
+// kCap: the logit soft cap is compiled in (a separate instantiation).
+template <int D, bool kCap>
 __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -574,12 +579,22 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
       // P = exp2(s * scale_log2 - lse2), packed pairs
       const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nl2 = f2_pack(-lse2, -lse2);
       float pv[kCols];
+      if constexpr (!kCap) {
 #pragma unroll
-      for (int c = 0; c < kCols; c += 2) {
-        float e0, e1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl2), e0, e1);
-        pv[c] = ex2_approx(e0);
-        pv[c + 1] = ex2_approx(e1);
+        for (int c = 0; c < kCols; c += 2) {
+          float e0, e1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl2), e0, e1);
+          pv[c] = ex2_approx(e0);
+          pv[c + 1] = ex2_approx(e1);
+        }
+      } else {
+        // soft cap: P = exp2(cap_log2 * t - lse2) with t = tanh(s * cap_scale);
+        // dQ only needs dS, so the factor 1 - t^2 goes into P here
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          const float t = tanh_fast(__uint_as_float(sv[c]) * p.cap_scale);
+          pv[c] = ex2_approx(fmaf(t, p.cap_log2, -lse2)) * fmaf(-t, t, 1.f);
+        }
       }
       if (label == 1) {
 #pragma unroll
@@ -775,7 +790,8 @@ struct DkvItems {
   }
 };
 
-template <int D>
+// kCap: the logit soft cap is compiled in (a separate instantiation).
+template <int D, bool kCap>
 __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -1046,31 +1062,50 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       reg_fence<kCols>(sv);
       // P = exp2((s*scale - LSE) * log2e): (LSE - s*scale) then times -log2e, packed pairs
       float pv[kCols];
+      if constexpr (!kCap) {
 #pragma unroll
-      for (int c4 = 0; c4 < kCols / 4; ++c4) {
-        const float4 l4 = lse4[c4];
-        const int c = c4 * 4;
-        float e0, e1, e2, e3;
-        f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nsc2, f2_pack(l4.x, l4.y)),
-                         nl2e2),
-                  e0, e1);
-        f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), nsc2, f2_pack(l4.z, l4.w)),
-                         nl2e2),
-                  e2, e3);
-        pv[c] = ex2_approx(e0);
-        pv[c + 1] = ex2_approx(e1);
-        pv[c + 2] = ex2_approx(e2);
-        pv[c + 3] = ex2_approx(e3);
-      }
-      if (label == 1) {
+        for (int c4 = 0; c4 < kCols / 4; ++c4) {
+          const float4 l4 = lse4[c4];
+          const int c = c4 * 4;
+          float e0, e1, e2, e3;
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nsc2, f2_pack(l4.x, l4.y)),
+                           nl2e2),
+                    e0, e1);
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), nsc2, f2_pack(l4.z, l4.w)),
+                           nl2e2),
+                    e2, e3);
+          pv[c] = ex2_approx(e0);
+          pv[c + 1] = ex2_approx(e1);
+          pv[c + 2] = ex2_approx(e2);
+          pv[c + 3] = ex2_approx(e3);
+        }
+        if (label == 1) {
 #pragma unroll
-        for (int c = 0; c < kCols; ++c)
-          if (!((allowed >> c) & 1ull)) pv[c] = 0.f;
-      }
-      {
+          for (int c = 0; c < kCols; ++c)
+            if (!((allowed >> c) & 1ull)) pv[c] = 0.f;
+        }
         uint32_t ppk[kCols / 2];
 #pragma unroll
         for (int c = 0; c < kCols / 2; ++c) ppk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+        tmem_st_cols<kCols / 2>(tmem + kDkvColST + col0 + lane_off, ppk);
+      } else {
+        // soft cap: P = exp2(cap_log2 * t - LSE * log2e), t = tanh(s * cap_scale);
+        // P^T goes to tensor memory for dV, and pv keeps P (1 - t^2) for dS
+        uint32_t ppk[kCols / 2];
+#pragma unroll
+        for (int c = 0; c < kCols; c += 2) {
+          const float t0 = tanh_fast(__uint_as_float(sv[c]) * p.cap_scale);
+          const float t1 = tanh_fast(__uint_as_float(sv[c + 1]) * p.cap_scale);
+          float p0 = ex2_approx(fmaf(t0, p.cap_log2, -s.lse[st][col0 + c] * kLog2e));
+          float p1 = ex2_approx(fmaf(t1, p.cap_log2, -s.lse[st][col0 + c + 1] * kLog2e));
+          if (label == 1) {
+            p0 = ((allowed >> c) & 1ull) ? p0 : 0.f;
+            p1 = ((allowed >> (c + 1)) & 1ull) ? p1 : 0.f;
+          }
+          ppk[c / 2] = pack_bf16x2(p0, p1);
+          pv[c] = p0 * fmaf(-t0, t0, 1.f);
+          pv[c + 1] = p1 * fmaf(-t1, t1, 1.f);
+        }
         tmem_st_cols<kCols / 2>(tmem + kDkvColST + col0 + lane_off, ppk);
       }
       tmem_wait_st();
@@ -1174,6 +1209,10 @@ bool make_maps(const bsa_bwd_args* a, CUtensorMap* tq, CUtensorMap* tk, CUtensor
 BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, uint32_t* err) {
   BwdParams p{};
   p.kv_splits = 1;
+  if (a->logits_soft_cap > 0.f) {
+    p.cap_scale = scale / a->logits_soft_cap;
+    p.cap_log2 = a->logits_soft_cap * 1.4426950408889634f;
+  }
   p.B = a->B;
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
@@ -1205,12 +1244,14 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
   BwdParams p = make_params(a, info, scale, err);
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
   p.n_tiles = a->B * a->Hkv * p.nK;
+  const bool cap = p.cap_scale != 0.f;
   const size_t smem = sizeof(DkvSmem<D>) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[cap]) {
+    cudaError_t e = cudaFuncSetAttribute(cap ? dkv_kernel<D, true> : dkv_kernel<D, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "set dkv smem size");
-    attr_set = true;
+    attr_set[cap] = true;
   }
   // With few KV tiles (MQA, short sequences) the q heads of a group are
   // split over several CTAs: the smallest divisor of the group that gives
@@ -1241,7 +1282,9 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
     p.part_dk = static_cast<float*>(ws);
     p.part_dv = p.part_dk + static_cast<size_t>(splits) * part_rows * D;
   }
-  cudaError_t e = launch_kernel(dkv_kernel<D>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
+  cudaError_t e =
+      cap ? launch_kernel(dkv_kernel<D, true>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p)
+          : launch_kernel(dkv_kernel<D, false>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess && splits > 1) {
     const int64_t n4 = part_rows * D / 4;
@@ -1266,19 +1309,23 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
   BwdParams p = make_params(a, info, scale, err);
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
   p.n_tiles = a->B * a->Hq * p.nQ;
+  const bool cap = p.cap_scale != 0.f;
   const size_t smem = sizeof(DqSmem<D>) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[cap]) {
+    cudaError_t e = cudaFuncSetAttribute(cap ? dq_kernel<D, true> : dq_kernel<D, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "set dq smem size");
-    attr_set = true;
+    attr_set[cap] = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
   if (schedule) {
     bsa_status st = tile_schedule(info, a->B, a->Hq, 1, 1, grid, &p.sched, &p.sched_stride);
     if (st != BSA_OK) return st;
   }
-  cudaError_t e = launch_kernel(dq_kernel<D>, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
+  cudaError_t e =
+      cap ? launch_kernel(dq_kernel<D, true>, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p)
+          : launch_kernel(dq_kernel<D, false>, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dq launch");
   return BSA_OK;

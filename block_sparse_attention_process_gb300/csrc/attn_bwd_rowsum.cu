@@ -6,6 +6,8 @@
 // HBM-bound: it reads 4*D bytes per row and writes 4.  Each row is split
 // over D/8 lanes that load 16 bytes of dO and 16 of O (coalesced, one
 // 128-byte line per 8 lanes), multiply in fp32 and reduce with shuffles.
+#include <cmath>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -40,7 +42,47 @@ __global__ void __launch_bounds__(256) rowsum_kernel(const uint4* __restrict__ d
   }
 }
 
+// Gradient of the attention sinks (extra logits z_j of every row's
+// normaliser, no value): dz_j = -sum over the rows of exp(z_j - LSE) * Dsum.
+// One CTA per 128-row query block of one (b, q head): one row per thread,
+// a block reduction per sink, then one atomic add per sink and CTA.
+__global__ void __launch_bounds__(128) dsink_kernel(const float* __restrict__ lse, const float* __restrict__ dsum,
+                                                    const float* __restrict__ sinks, float* __restrict__ dsinks,
+                                                    int32_t Hq, int32_t Hkv, int64_t Sq, int32_t n_sinks,
+                                                    int32_t per_kv) {
+  griddep_launch_dependents();
+  griddep_wait();  // Dsum comes from the rowsum kernel
+  __shared__ float part[4];
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 128 + threadIdx.x;
+  const int32_t hq = static_cast<int32_t>((row / Sq) % Hq);
+  const int32_t srow = per_kv ? hq / (Hq / Hkv) : 0;
+  const float l = lse[row], d = dsum[row];
+  for (int32_t j = 0; j < n_sinks; ++j) {
+    const float z = sinks[srow * n_sinks + j];
+    float c = (l == -INFINITY) ? 0.f : -expf(z - l) * d;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(&dsinks[srow * n_sinks + j], (part[0] + part[1]) + (part[2] + part[3]));
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+bsa_status dsink_launch(const bsa_bwd_args* a, cudaStream_t stream) {
+  if (a->num_sinks <= 0 || !a->dsinks) return BSA_OK;
+  const int32_t srows = a->sinks_per_kv_head ? a->Hkv : 1;
+  cudaError_t e = cudaMemsetAsync(a->dsinks, 0, sizeof(float) * srows * a->num_sinks, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clear dsinks");
+  const int64_t blocks = static_cast<int64_t>(a->B) * a->Hq * a->S_q / 128;
+  e = launch_kernel(dsink_kernel, dim3(static_cast<unsigned>(blocks)), dim3(128), 0, stream, a->lse, a->dsum,
+                    a->sinks, a->dsinks, a->Hq, a->Hkv, a->S_q, a->num_sinks, a->sinks_per_kv_head ? 1 : 0);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "dsink launch");
+  return BSA_OK;
+}
 
 bsa_status rowsum_launch(const bsa_bwd_args* a, cudaStream_t stream) {
   const int64_t n_rows = static_cast<int64_t>(a->B) * a->Hq * a->S_q;
@@ -53,7 +95,7 @@ bsa_status rowsum_launch(const bsa_bwd_args* a, cudaStream_t stream) {
                               : launch_kernel(rowsum_kernel<64>, dim3(grid), dim3(256), 0, stream, dout, out, a->dsum, n_rows);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "rowsum launch");
-  return BSA_OK;
+  return dsink_launch(a, stream);
 }
 
 }  // namespace bsa

@@ -108,6 +108,12 @@ struct FwdParams {
   // (natural-log units) and normaliser instead of O and LSE.
   int32_t kv_lo, kv_hi;
   int32_t partial;
+  // soft cap c (off when cap_scale == 0): scaled score s -> c*tanh(s/c),
+  // i.e. log2 units cap_log2 * tanh(raw * cap_scale), cap_scale = scale / c
+  float cap_log2, cap_scale;
+  // sinks: n_sinks logits per row in the normaliser; row sinks_kv ? kv head : 0
+  const float* sinks;
+  int32_t n_sinks, sinks_kv;
   float* o_acc;
   float* m_out;
   float* l_out;
@@ -115,7 +121,9 @@ struct FwdParams {
   uint64_t wait_ns;
 };
 
-template <int D>
+// kX: the logit soft cap and / or attention sinks are compiled in (a
+// separate instantiation, so that the plain kernel keeps its code).
+template <int D, bool kX>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
@@ -236,7 +244,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
           for (int v = lane; v < 128 * D / 8; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-          for (int r = lane; r < 128; r += 32) p.lse[out_row + r] = -INFINITY;
+          // only the sinks are left in the normaliser
+          float lse0 = -INFINITY;
+          if (kX && p.n_sinks > 0) {
+            const float* z = p.sinks + (p.sinks_kv ? (t_hq / (p.Hq / p.Hkv)) * p.n_sinks : 0);
+            float zm = -INFINITY, zs = 0.f;
+            for (int j = 0; j < p.n_sinks; ++j) zm = fmaxf(zm, z[j]);
+            for (int j = 0; j < p.n_sinks; ++j) zs += expf(z[j] - zm);
+            lse0 = zm + logf(zs);
+          }
+          for (int r = lane; r < 128; r += 32) p.lse[out_row + r] = lse0;
         }
         continue;
       }
@@ -550,6 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = -INFINITY;
         l = 0.f;
         exec = 0;
+        if (kX && p.n_sinks > 0) {
+          // the sinks open the row's running maximum and (in part 0) its sum
+          const int32_t hq = static_cast<int32_t>((static_cast<int64_t>(bi.w) / p.Sq) % p.Hq);
+          const float* z = p.sinks + (p.sinks_kv ? (hq / (p.Hq / p.Hkv)) * p.n_sinks : 0);
+          for (int j = 0; j < p.n_sinks; ++j) m = fmaxf(m, z[j] * 1.4426950408889634f);
+          if (part == 0)
+            for (int j = 0; j < p.n_sinks; ++j) l += ex2_approx(z[j] * 1.4426950408889634f - m);
+        }
         // q_sequence is consecutive within a query block: row r has q_sequence[128 i] + r
         if (p.mi.kind != BSA_MASK_DENSE)
           key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(static_cast<int32_t>(bi.z)) + r,
@@ -612,7 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = s.xmax[n & 1u][0][r];
 #pragma unroll
       for (int q = 1; q < kParts; ++q) mx = fmaxf(mx, s.xmax[n & 1u][q][r]);
-      const float m_blk = mx * scale_log2;
+      // tanh is increasing: the capped maximum is the cap of the maximum
+      const float m_blk = (!kX || p.cap_scale == 0.f) ? mx * scale_log2
+                          : (mx == -INFINITY ? -INFINITY : p.cap_log2 * tanh_fast(mx * p.cap_scale));
       const float m_cand = fmaxf(m, m_blk);
       const bool switch_ref = m_cand > m + kRescaleThreshold;
       const bool warp_switch = __any_sync(0xffffffffu, switch_ref);  // same rows, same values in every part
@@ -628,14 +655,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int a = 0; a < 4; ++a) acc[a] = f2_pack(0.f, 0.f);
       uint32_t pk[kCols / 2];
+      if (!kX || p.cap_scale == 0.f) {
 #pragma unroll
-      for (int c = 0; c < kCols / 2; ++c) {
-        const uint64_t e2 = f2_fma(f2_pack(__uint_as_float(xu[2 * c]), __uint_as_float(xu[2 * c + 1])), sc2, nm2);
-        float e0, e1;
-        f2_unpack(e2, e0, e1);
-        const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-        acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
-        pk[c] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < kCols / 2; ++c) {
+          const uint64_t e2 = f2_fma(f2_pack(__uint_as_float(xu[2 * c]), __uint_as_float(xu[2 * c + 1])), sc2, nm2);
+          float e0, e1;
+          f2_unpack(e2, e0, e1);
+          const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+          acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+      } else {
+        // soft cap: exp2(cap_log2 * tanh(s * cap_scale) - m); masked (-inf) scores stay at 0
+#pragma unroll
+        for (int c = 0; c < kCols / 2; ++c) {
+          const float x0 = __uint_as_float(xu[2 * c]), x1 = __uint_as_float(xu[2 * c + 1]);
+          float e0 = fmaf(tanh_fast(x0 * p.cap_scale), p.cap_log2, -m_use);
+          float e1 = fmaf(tanh_fast(x1 * p.cap_scale), p.cap_log2, -m_use);
+          e0 = x0 == -INFINITY ? -INFINITY : e0;
+          e1 = x1 == -INFINITY ? -INFINITY : e1;
+          const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+          acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
+          pk[c] = pack_bf16x2(p0, p1);
+        }
       }
       const uint64_t acc01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
       float rs0, rs1;
@@ -707,6 +749,9 @@ struct FwdCall {
   float* lse;
   float *o_acc, *m, *l;
   int32_t kv_lo, kv_hi, partial;
+  float cap;
+  const float* sinks;
+  int32_t n_sinks, sinks_kv;
 };
 
 template <int D>
@@ -735,22 +780,32 @@ bsa_status launch_fwd(const FwdCall& c, const bsa_mask_info* info, float scale, 
   p.kv_lo = c.kv_lo;
   p.kv_hi = c.kv_hi;
   p.partial = c.partial;
+  if (c.cap > 0.f) {
+    p.cap_scale = scale / c.cap;
+    p.cap_log2 = c.cap * 1.4426950408889634f;
+  }
+  p.sinks = c.sinks;
+  p.n_sinks = c.n_sinks;
+  p.sinks_kv = c.sinks_kv;
   p.mi = mask_info_dev(info);
   p.n_tiles = c.B * c.Hq * p.nQ;
   p.err = device_error_word();
   p.wait_ns = wait_limit_ns();
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
+  const bool xform = p.cap_scale != 0.f || p.n_sinks > 0;
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[xform]) {
+    cudaError_t e = cudaFuncSetAttribute(xform ? fwd_kernel<D, true> : fwd_kernel<D, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "set forward smem size");
-    attr_set = true;
+    attr_set[xform] = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
   bsa_status st = tile_schedule(info, c.B, c.Hq, 1, 1, grid, &p.sched, &p.sched_stride);
   if (st != BSA_OK) return st;
-  cudaError_t e = launch_kernel(fwd_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p);
+  cudaError_t e = xform ? launch_kernel(fwd_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p)
+                        : launch_kernel(fwd_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return BSA_OK;
@@ -778,6 +833,10 @@ bsa_status fwd_launch(const bsa_fwd_args* a, const bsa_mask_info* info, float sc
   c.kv_lo = 0;
   c.kv_hi = info->cols;
   c.partial = 0;
+  c.cap = a->logits_soft_cap;
+  c.sinks = a->num_sinks > 0 ? a->sinks : nullptr;
+  c.n_sinks = a->num_sinks > 0 ? a->num_sinks : 0;
+  c.sinks_kv = a->sinks_per_kv_head ? 1 : 0;
   return dispatch(c, a->D, info, scale, stream);
 }
 
@@ -798,6 +857,7 @@ bsa_status fwd_partial_launch(const bsa_fwd_partial_args* a, const bsa_mask_info
   c.kv_lo = static_cast<int32_t>(a->kv_offset / 128);
   c.kv_hi = static_cast<int32_t>((a->kv_offset + a->S_kv_shard) / 128);
   c.partial = 1;
+  c.cap = a->logits_soft_cap;
   return dispatch(c, a->D, info, scale, stream);
 }
 

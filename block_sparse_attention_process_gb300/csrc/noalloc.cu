@@ -73,6 +73,10 @@ bsa_status check(const bsa_bwd_args* a, const bsa_mask_info* fwd_info, const bsa
     if (!p) return fail(BSA_ERR_INVALID_ARG, "a tensor pointer is null");
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(BSA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!(a->logits_soft_cap >= 0.f) || std::isinf(a->logits_soft_cap))
+    return fail(BSA_ERR_INVALID_ARG, "logits_soft_cap must be finite and >= 0");
+  if (a->num_sinks < 0 || a->num_sinks > 64) return fail(BSA_ERR_UNSUPPORTED, "num_sinks must be in 0..64");
+  if (a->num_sinks > 0 && !a->sinks) return fail(BSA_ERR_INVALID_ARG, "sinks is null");
   const bsa_mask_info* infos[2] = {fwd_info, dkv_info};
   const int32_t orient[2] = {BSA_ORIENT_FWD, BSA_ORIENT_DKV};
   for (int i = 0; i < 2; ++i) {

@@ -397,10 +397,20 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// tanh for the logit soft cap, from its definition 1 - 2 / (1 + e^{2x}):
+// one exp2 and one fast divide, absolute error ~1e-6 (the hardware
+// tanh.approx, at ~5e-4 relative, would be too coarse for the logsumexp).
+// |x| is clamped at 16, where tanh is 1 in fp32.
+__device__ __forceinline__ float tanh_fast(float x) {
+  const float xc = fminf(fmaxf(x, -16.f), 16.f);
+  return 1.f - __fdividef(2.f, 1.f + ex2_approx(xc * 2.8853900817779268f));
 }
 
 __device__ __forceinline__ uint32_t elect_one_lane() {

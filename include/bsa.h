@@ -143,6 +143,18 @@ typedef struct {
   int32_t B, Hq, Hkv, D;
   int64_t S_q, S_kv;
   float softmax_scale; /* NaN selects 1/sqrt(D) */
+  /* Optional score transforms (the logits_soft_cap and softmax_aux arguments
+   * of the EasyDeL blocksparse_attention operator; zero-initialised = off):
+   * logits_soft_cap c > 0 maps each visible scaled score s to c*tanh(s/c);
+   * sinks are num_sinks extra logits per row that enter the normaliser (and
+   * the maximum) but carry no value, fp32 on the device, [Hkv, num_sinks]
+   * (q head h uses row h / (Hq/Hkv)) when sinks_per_kv_head is 1, else
+   * [num_sinks] shared by all heads.  LSE includes the sinks; a row with no
+   * visible key gets O = 0 and LSE = log(sum_j exp(z_j)). */
+  float logits_soft_cap;
+  const float* sinks;
+  int32_t num_sinks;   /* 0..64 */
+  int32_t sinks_per_kv_head;
 } bsa_fwd_args;
 
 /* Block-sparse forward ("What is splash attention and how is it different
@@ -183,6 +195,8 @@ typedef struct {
   int64_t S_kv_shard;   /* multiple of 128 */
   int64_t kv_offset;    /* the shard's first key on the MaskInfo's key axis, multiple of 128 */
   float softmax_scale;  /* NaN selects 1/sqrt(D) */
+  float logits_soft_cap; /* as in bsa_fwd_args (sinks are not accepted for shards: they would
+                            enter every shard's normaliser) */
 } bsa_fwd_partial_args;
 
 /* Forward over one key shard: the same kernel as bsa_fwd, walking only the
@@ -222,6 +236,17 @@ typedef struct {
   int64_t S_q, S_kv;
   float softmax_scale;   /* NaN selects 1/sqrt(D) */
   int32_t grad_fp32;     /* 0: dq/dk/dv are bf16; 1: fp32 */
+  /* The forward's score transforms (see bsa_fwd_args); lse must come from a
+   * forward with the same ones.  With the cap, dS is taken through
+   * c*tanh(s/c) (times 1 - tanh^2).  With sinks and a non-null dsinks, the
+   * sinks' gradient -sum over rows of exp(z_j - LSE) * Dsum is written to
+   * dsinks (fp32, the sinks' shape; accumulated with atomics, so the
+   * summation order, and the last bits, vary between runs). */
+  float logits_soft_cap;
+  const float* sinks;
+  float* dsinks;
+  int32_t num_sinks;
+  int32_t sinks_per_kv_head;
 } bsa_bwd_args;
 
 /* Backward ("Flash Attention on a TPU, Line by Line": "Why does the TPU flash
@@ -231,7 +256,8 @@ typedef struct {
  * MaskInfo of the same mask), then bsa_bwd_dq with `fwd_info`. */
 BSA_API bsa_status bsa_bwd(const bsa_bwd_args* args, const bsa_mask_info* fwd_info, const bsa_mask_info* dkv_info,
                    bsa_stream stream);
-/* dsum[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d] (fp32). */
+/* dsum[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d] (fp32); with sinks and
+ * dsinks, also the sinks' gradient (it needs Dsum and LSE only). */
 BSA_API bsa_status bsa_bwd_rowsum(const bsa_bwd_args* args, bsa_stream stream);
 /* dK, dV: grid over (b, kv head, key block), queries innermost.  When
  * B * Hkv * (S_kv / 128) is small next to the number of SMs (MQA, short
