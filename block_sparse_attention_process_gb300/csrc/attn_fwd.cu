@@ -71,6 +71,9 @@ struct __align__(1024) FwdSmem {
   uint8_t q[2][kTileBytes];
   uint8_t k[kStagesK][kTileBytes];
   uint8_t v[kStagesV][kTileBytes];
+  // bf16 output staging of the epilogue warps: 32 rows x 64 columns each
+  // (128-byte swizzle, the layout of the output tensor map's box)
+  uint8_t ostage[4][32 * 128];
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kStagesK], k_empty[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
@@ -91,6 +94,8 @@ struct __align__(1024) FwdSmem {
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+
+static_assert(sizeof(FwdSmem<128>) + 1024 <= 232448, "forward shared memory exceeds 227 KB per CTA");
 
 struct FwdParams {
   int32_t B, Hq, Hkv, nQ, nK;
@@ -126,7 +131,8 @@ struct FwdParams {
 template <int D, bool kX>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = FwdSmem<D>;
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -464,52 +470,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
       const int64_t orow = static_cast<int64_t>(row0) + r;
-      // O / l in bf16, or (a key shard) the unnormalised fp32 accumulator
-      auto emit_bf16 = [&](const uint32_t* v, int c) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint4 o4;
-          o4.x = pack_bf16x2(__uint_as_float(v[8 * e + 0]) * inv_l, __uint_as_float(v[8 * e + 1]) * inv_l);
-          o4.y = pack_bf16x2(__uint_as_float(v[8 * e + 2]) * inv_l, __uint_as_float(v[8 * e + 3]) * inv_l);
-          o4.z = pack_bf16x2(__uint_as_float(v[8 * e + 4]) * inv_l, __uint_as_float(v[8 * e + 5]) * inv_l);
-          o4.w = pack_bf16x2(__uint_as_float(v[8 * e + 6]) * inv_l, __uint_as_float(v[8 * e + 7]) * inv_l);
-          dst[c * 4 + e] = o4;
-        }
-      };
-      auto emit_acc = [&](const uint32_t* v, int c) {
+      if (p.partial) {
+        // (a key shard) the unnormalised fp32 accumulator, 16 columns at a time
         uint4* dst = reinterpret_cast<uint4*>(p.o_acc + orow * D);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dst[c * 8 + e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-      };
-      // chunks of 32 columns, the next one in flight while this one is
-      // stored (straight-line code up to each wait)
-      auto drain = [&](auto emit) {
-        uint32_t va[32], vb[32];
-        tmem_ld32(obase, va);
-        tmem_wait_ld();
-        reg_fence32(va);
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t va[16];
+          tmem_ld16(obase + c * 16, va);
+          tmem_wait_ld();
+          reg_fence16(va);
 #pragma unroll
-        for (int c = 0; c < D / 32; c += 2) {
-          if (c + 1 < D / 32) tmem_ld32(obase + (c + 1) * 32, vb);
-          emit(va, c);
-          if (c + 1 < D / 32) {
+          for (int e = 0; e < 4; ++e) dst[c * 4 + e] = make_uint4(va[4 * e], va[4 * e + 1], va[4 * e + 2], va[4 * e + 3]);
+        }
+        // (every load of this tile's O has completed by the last wait)
+        tc_fence_before();
+        mbar_arrive(&s.o_empty);
+      } else {
+        // O / l in bf16 through this warp's staging buffer and a TMA store of
+        // [32 rows, 64 columns] per half: the stores are coalesced and off the
+        // load/store unit.  The second half waits in registers while the first
+        // one's store reads the buffer, and O is released to the next tile's
+        // P V as soon as both halves are out of tensor memory.
+        uint8_t* stage = s.ostage[quarter];
+        const int32_t grow = static_cast<int32_t>(row0) + quarter * 32;  // global row of lane 0
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t va[16];
+            tmem_ld16(obase + h * 64 + c * 16, va);
             tmem_wait_ld();
-            reg_fence32(vb);
-            if (c + 2 < D / 32) tmem_ld32(obase + (c + 2) * 32, va);
-            emit(vb, c + 1);
-            if (c + 2 < D / 32) {
-              tmem_wait_ld();
-              reg_fence32(va);
-            }
+            reg_fence16(va);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              pk[c * 8 + j] = pack_bf16x2(__uint_as_float(va[2 * j]) * inv_l, __uint_as_float(va[2 * j + 1]) * inv_l);
+          }
+          if (h == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(&s.o_empty);
+          }
+          // the previous store out of this buffer has finished reading it
+          if (lane == 0) tma_store_wait_read();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((j ^ (lane & 7)) * 16)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_o, stage, h * 64, grow);
+            tma_store_commit();
           }
         }
-      };
-      if (p.partial) drain(emit_acc);
-      else drain(emit_bf16);
-      // (every load of this tile's O has completed by the last wait)
-      tc_fence_before();
-      mbar_arrive(&s.o_empty);
+      }
       if (p.partial) {
         p.m_out[orow] = l_row > 0.f ? mrow * 0.69314718055994530942f : -INFINITY;
         p.l_out[orow] = l_row;
@@ -517,6 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[orow] = l_row > 0.f ? (mrow + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
       }
     }
+    // the staging buffers stay valid until every TMA store has read them
+    if (lane == 0) tma_store_wait_all();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax (kParts warpgroups)
     // Warpgroup `part` takes score columns [kCols*part, kCols*part + kCols)
@@ -756,13 +773,18 @@ struct FwdCall {
 
 template <int D>
 bsa_status launch_fwd(const FwdCall& c, const bsa_mask_info* info, float scale, cudaStream_t stream) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint64_t q_rows = static_cast<uint64_t>(c.B) * c.Hq * c.Sq;
   const uint64_t kv_rows = static_cast<uint64_t>(c.B) * c.Hkv * c.Skv;
   if (!make_tmap_bf16_2d(&tq, c.q, q_rows, D, D * 2, 128, 64) ||
       !make_tmap_bf16_2d(&tk, c.k, kv_rows, D, D * 2, 128, 64) ||
       !make_tmap_bf16_2d(&tv, c.v, kv_rows, D, D * 2, 128, 64))
     return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a Q/K/V description");
+  // the bf16 output, stored in [32 rows, 64 columns] boxes (a key shard
+  // writes fp32 with plain stores: the Q map stands in, unused)
+  if (c.partial) to = tq;
+  else if (!make_tmap_bf16_2d(&to, c.o, q_rows, D, D * 2, 32, 64))
+    return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected the output description");
   FwdParams p{};
   p.B = c.B;
   p.Hq = c.Hq;
@@ -804,8 +826,8 @@ bsa_status launch_fwd(const FwdCall& c, const bsa_mask_info* info, float scale, 
   const int grid = std::min(p.n_tiles, num_sms());
   bsa_status st = tile_schedule(info, c.B, c.Hq, 1, 1, grid, &p.sched, &p.sched_stride);
   if (st != BSA_OK) return st;
-  cudaError_t e = xform ? launch_kernel(fwd_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p)
-                        : launch_kernel(fwd_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, p);
+  cudaError_t e = xform ? launch_kernel(fwd_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, to, p)
+                        : launch_kernel(fwd_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, to, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return BSA_OK;
