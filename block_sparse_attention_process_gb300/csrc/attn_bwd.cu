@@ -94,6 +94,21 @@ struct BwdParams {
   uint64_t wait_ns;
 };
 
+// One row of 32 fp32 values times `mul`, as bf16, into row `r` of a
+// [32 rows, 64 bytes] staging box in the 64-byte swizzle of its tensor map
+// (conflict-free: the 8 rows of a quarter warp cover all 32 banks).
+__device__ __forceinline__ void stage_row_sw64(uint8_t* box, int r, const uint32_t* v, float mul) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 o;
+    o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * mul, __uint_as_float(v[8 * j + 1]) * mul);
+    o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * mul, __uint_as_float(v[8 * j + 3]) * mul);
+    o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * mul, __uint_as_float(v[8 * j + 5]) * mul);
+    o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * mul, __uint_as_float(v[8 * j + 7]) * mul);
+    *reinterpret_cast<uint4*>(box + r * 64 + ((j ^ ((r >> 1) & 3)) * 16)) = o;
+  }
+}
+
 __device__ __forceinline__ void store_row(void* base, int fp32, int64_t row, int D, const uint32_t* v, int c0,
                                           float mul) {
   // 32 consecutive fp32 accumulator values of one row -> output columns [c0, c0+32)
@@ -666,7 +681,10 @@ struct __align__(1024) DkvSmem {
   uint8_t dout[kDkvStages][kTile];
   float lse[kDkvStages][128];
   float dsum[kDkvStages][128];
-  uint64_t kv_full, kv_empty;
+  uint64_t k_full, k_empty, v_full, v_empty;
+  // in_empty: the MMA warp's commit after an item's dK, plus one arrival per
+  // elementwise warp (at a tile's last item, once its tensor stores out of
+  // the item's Q / dO buffers have read them; otherwise from the MMA warp)
   uint64_t in_full[kDkvStages], in_empty[kDkvStages];
   uint64_t st_full, dpt_full, p_full, ds_full;
   uint64_t acc_full, acc_empty, drain;
@@ -795,6 +813,7 @@ template <int D, bool kCap>
 __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = DkvSmem<D>;
@@ -806,11 +825,13 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
-    mbar_init(&s.kv_full, 1);
-    mbar_init(&s.kv_empty, 1);
+    mbar_init(&s.k_full, 1);
+    mbar_init(&s.k_empty, 1);
+    mbar_init(&s.v_full, 1);
+    mbar_init(&s.v_empty, 1);
     for (int i = 0; i < kDkvStages; ++i) {
       mbar_init(&s.in_full[i], 1);
-      mbar_init(&s.in_empty[i], 1);
+      mbar_init(&s.in_empty[i], 1 + 4 * DkvShape<D>::kParts);
     }
     mbar_init(&s.st_full, 1);
     mbar_init(&s.dpt_full, 1);
@@ -844,28 +865,12 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       tma_prefetch_desc(&tm_do);
       const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      uint32_t kv_loads = 0, in_loads = 0;
+      uint32_t k_loads = 0, v_loads = 0, in_loads = 0;
       bool ok = true;
       DkvTile t;
       for (int32_t kt = 0; ok && dkv_tile(p, kt, t); ++kt) {
         if (t.total == 0) continue;
-        if (kv_loads >= 1 && !mbar_wait(&s.kv_empty, (kv_loads - 1) & 1u, wc)) { ok = false; break; }
-        mbar_arrive_expect_tx(&s.kv_full, 2 * kTile);
         const int32_t krow = static_cast<int32_t>((static_cast<int64_t>(t.b) * p.Hkv + t.g) * p.Skv + t.j * 128);
-        for (int c = 0; c < kChunks; ++c) {
-          tma_load_2d(s.k + c * 16384, &tm_k, &s.kv_full, c * 64, krow, pol_kv);
-          tma_load_2d(s.v + c * 16384, &tm_v, &s.kv_full, c * 64, krow, pol_kv);
-        }
-        ++kv_loads;
-        // warm L2 with this CTA's next tile's K and V
-        DkvTile t2;
-        for (int32_t k2 = kt + 1; dkv_tile(p, k2, t2); ++k2) {
-          if (t2.total == 0) continue;
-          const int64_t row2 = (static_cast<int64_t>(t2.b) * p.Hkv + t2.g) * p.Skv + t2.j * 128;
-          prefetch_l2(static_cast<const uint8_t*>(p.kp) + row2 * D * 2, 128 * D * 2);
-          prefetch_l2(static_cast<const uint8_t*>(p.vp) + row2 * D * 2, 128 * D * 2);
-          break;
-        }
         DkvItems it;
         it.init(p, t);
         int32_t hq;
@@ -888,12 +893,35 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           bulk_load(s.lse[st], p.lse + qrow, 512, &s.in_full[st]);
           bulk_load(s.dsum[st], p.dsum + qrow, 512, &s.in_full[st]);
           ++in_loads;
+          if (x > 0) continue;
+          // The tile's K and V follow its first query block, so that this
+          // block's loads do not wait for the previous tile's last MMAs: K is
+          // free once the previous tile's last S^T has completed, V once its
+          // last dP^T has.
+          if (k_loads >= 1 && !mbar_wait(&s.k_empty, (k_loads - 1) & 1u, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.k_full, kTile);
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(s.k + c * 16384, &tm_k, &s.k_full, c * 64, krow, pol_kv);
+          ++k_loads;
+          if (v_loads >= 1 && !mbar_wait(&s.v_empty, (v_loads - 1) & 1u, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.v_full, kTile);
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(s.v + c * 16384, &tm_v, &s.v_full, c * 64, krow, pol_kv);
+          ++v_loads;
+          // warm L2 with this CTA's next tile's K and V
+          DkvTile t2;
+          for (int32_t k2 = kt + 1; dkv_tile(p, k2, t2); ++k2) {
+            if (t2.total == 0) continue;
+            const int64_t row2 = (static_cast<int64_t>(t2.b) * p.Hkv + t2.g) * p.Skv + t2.j * 128;
+            prefetch_l2(static_cast<const uint8_t*>(p.kp) + row2 * D * 2, 128 * D * 2);
+            prefetch_l2(static_cast<const uint8_t*>(p.vp) + row2 * D * 2, 128 * D * 2);
+            break;
+          }
         }
       }
       if (!ok) {
         uint32_t dummy_abort = 0;
         WaitCtl dw{nullptr, &dummy_abort, p.wait_ns};
-        if (kv_loads) (void)mbar_wait(&s.kv_full, (kv_loads - 1) & 1u, dw);
+        if (k_loads) (void)mbar_wait(&s.k_full, (k_loads - 1) & 1u, dw);
+        if (v_loads) (void)mbar_wait(&s.v_full, (v_loads - 1) & 1u, dw);
         for (uint32_t i = (in_loads > kDkvStages ? in_loads - kDkvStages : 0); i < in_loads; ++i)
           (void)mbar_wait(&s.in_full[i % kDkvStages], (i / kDkvStages) & 1u, dw);
       }
@@ -915,12 +943,15 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       DkvTile t;
       for (int32_t kt = 0; dkv_tile(p, kt, t); ++kt) total += static_cast<uint32_t>(t.total);
     }
-    uint32_t kv_uses = 0, acc_uses = 0;
+    uint32_t k_uses = 0, v_uses = 0, acc_uses = 0;
     bool ok = true;
     // S^T(n+1) is issued right after dV(n) (which reads P^T(n) from the same
     // columns first), so the tensor cores compute the next scores while the
     // elementwise warps work on dS^T(n); dP^T(n+1) follows dK(n) likewise.
     // Order: S^T(0) dP^T(0) | dV(0) S^T(1) dK(0) dP^T(1) | dV(1) S^T(2) ...
+    // At a tile's last item n, S^T(n+1) waits until after dK(n): the
+    // accumulators go to the epilogue without waiting for the next tile's
+    // loads.
     uint32_t flags = 0;  // first/last bits of items n and n+1, two per item
     auto item_flags = [&](uint32_t k) -> bool {
       const uint32_t st = k % kDkvStages;
@@ -928,9 +959,9 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[k % kInfoRing].x, 0);
       const uint32_t sh = 2u * (k & 7u);
       flags = (flags & ~(3u << sh)) | (((info >> 20) & 3u) << sh);
-      if ((info >> 20) & 1u) {  // first item of a tile: its K and V
-        if (!mbar_wait_warp(&s.kv_full, kv_uses & 1u, wc)) return false;
-        ++kv_uses;
+      if ((info >> 20) & 1u) {  // first item of a tile: its K
+        if (!mbar_wait_warp(&s.k_full, k_uses & 1u, wc)) return false;
+        ++k_uses;
       }
       tc_fence_after();
       return true;
@@ -943,8 +974,15 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         mma_ss_elect(tmem + kDkvColST, kdesc + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.st_full);
+      // K is read by the S^T MMAs only
+      if ((flags >> (2u * (k & 7u))) & 2u) mma_commit_elect(&s.k_empty);
     };
-    auto issue_dpt = [&](uint32_t k) {
+    auto issue_dpt = [&](uint32_t k) -> bool {
+      if ((flags >> (2u * (k & 7u))) & 1u) {  // first item of a tile: its V
+        if (!mbar_wait_warp(&s.v_full, v_uses & 1u, wc)) return false;
+        ++v_uses;
+        tc_fence_after();
+      }
       const uint64_t dod = dodesc0 + (k % kDkvStages) * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -952,14 +990,15 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         mma_ss_elect(tmem + kDkvColDP, vdesc + off, dod + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.dpt_full);
-      // K and V are read by the S^T / dP^T MMAs only
-      if ((flags >> (2u * (k & 7u))) & 2u) mma_commit_elect(&s.kv_empty);
+      // V is read by the dP^T MMAs only
+      if ((flags >> (2u * (k & 7u))) & 2u) mma_commit_elect(&s.v_empty);
+      return true;
     };
     if (total > 0) {
       ok = item_flags(0);
       if (ok) {
         issue_st(0);
-        issue_dpt(0);
+        ok = issue_dpt(0);
       }
     }
     for (uint32_t n = 0; ok && n < total; ++n) {
@@ -978,7 +1017,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
                      domn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
       // next item's S^T over the P^T columns the dV MMA has just read
-      if (more) {
+      if (more && !last) {
         if (!item_flags(n + 1)) { ok = false; break; }
         issue_st(n + 1);
       }
@@ -995,9 +1034,20 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       if (last) {
         mma_commit_elect(&s.acc_full);
         ++acc_uses;
+      } else if (lane == 0) {
+        // the elementwise warps' share of in_empty (they only hold the Q / dO
+        // buffers of a tile's last item, for the epilogue's tensor stores)
+        mbar_arrive_cnt(&s.in_empty[st], 4 * DkvShape<D>::kParts);
       }
-      // next item's dP^T over the dS^T columns the dK MMA has just read
-      if (more) issue_dpt(n + 1);
+      __syncwarp();
+      if (more) {
+        if (last) {
+          if (!item_flags(n + 1)) { ok = false; break; }
+          issue_st(n + 1);
+        }
+        // next item's dP^T over the dS^T columns the dK MMA has just read
+        if (!issue_dpt(n + 1)) { ok = false; break; }
+      }
     }
     mma_commit_elect(&s.drain);
     uint32_t dummy_abort = 0;
@@ -1144,23 +1194,55 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       if (!last) continue;
       if (!mbar_wait_warp(&s.acc_full, acc_uses & 1u, wc)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < kPartD / 32; ++c) {
+      static_assert(kPartD == 32, "one 32-column slice of dK and dV per thread");
+      const bool sp = p.kv_splits > 1;
+      if (!sp && !p.grad_fp32) {
+        // bf16 dV and dK through shared memory: the last item's dO and Q
+        // buffers are free (its MMAs have completed) and stay the
+        // elementwise warps' until each releases them on in_empty.  A warp's
+        // [32 keys, 32 columns] of each goes out in one tensor store.
+        uint8_t* stv = s.dout[st] + (warp - 4) * 2048;
+        uint8_t* stk = s.q[st] + (warp - 4) * 2048;
         uint32_t v[32];
-        tmem_ld32(tmem + kDkvColDV + part * kPartD + c * 32 + lane_off, v);
+        tmem_ld32(tmem + kDkvColDV + part * kPartD + lane_off, v);
         tmem_wait_ld();
         reg_fence32(v);
-        const bool sp = p.kv_splits > 1;
-        store_row(sp ? p.part_dv : p.dv, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD + c * 32, 1.f);
-        tmem_ld32(tmem + kDkvColDK + part * kPartD + c * 32 + lane_off, v);
+        stage_row_sw64(stv, lane, v, 1.f);
+        tmem_ld32(tmem + kDkvColDK + part * kPartD + lane_off, v);
         tmem_wait_ld();
         reg_fence32(v);
-        store_row(sp ? p.part_dk : p.dk, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD + c * 32, p.scale);
+        stage_row_sw64(stk, lane, v, p.scale);
+        tc_fence_before();
+        mbar_arrive(&s.acc_empty);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t row0 = static_cast<int32_t>(krow - lane);  // key row of this warp's lane 0
+          tma_store_2d(&tm_dv, stv, part * kPartD, row0);
+          tma_store_2d(&tm_dk, stk, part * kPartD, row0);
+          tma_store_commit();
+          tma_store_wait_read();
+          mbar_arrive(&s.in_empty[st]);
+        }
+        __syncwarp();
+      } else {
+        uint32_t v[32];
+        tmem_ld32(tmem + kDkvColDV + part * kPartD + lane_off, v);
+        tmem_wait_ld();
+        reg_fence32(v);
+        store_row(sp ? p.part_dv : p.dv, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD, 1.f);
+        tmem_ld32(tmem + kDkvColDK + part * kPartD + lane_off, v);
+        tmem_wait_ld();
+        reg_fence32(v);
+        store_row(sp ? p.part_dk : p.dk, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD, p.scale);
+        tc_fence_before();
+        mbar_arrive(&s.acc_empty);
+        if (lane == 0) mbar_arrive(&s.in_empty[st]);
       }
-      tc_fence_before();
-      mbar_arrive(&s.acc_empty);
       ++acc_uses;
     }
+    // every tensor store has completed before the CTA exits
+    if (lane == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
@@ -1239,7 +1321,7 @@ BwdParams make_params(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
 template <int D>
 bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
                       uint32_t* err, bool schedule) {
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_maps(a, &tq, &tk, &tv, &tdo)) return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor");
   BwdParams p = make_params(a, info, scale, err);
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
@@ -1270,6 +1352,16 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
   }
   p.kv_splits = splits;
   p.part_rows = part_rows;
+  // bf16 dK / dV leave through tensor stores of [32 keys, 32 columns]; fp32
+  // outputs and split partials use plain stores (the Q map stands in, unused)
+  if (splits == 1 && !a->grad_fp32) {
+    if (!make_tmap_bf16_2d_sw64(&tdk, a->dk, part_rows, D, D * 2, 32) ||
+        !make_tmap_bf16_2d_sw64(&tdv, a->dv, part_rows, D, D * 2, 32))
+      return fail(BSA_ERR_CUDA, "cuTensorMapEncodeTiled rejected the dK / dV description");
+  } else {
+    tdk = tq;
+    tdv = tq;
+  }
   const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(p.n_tiles) * splits, num_sms()));
   if (schedule) {
     bsa_status st = tile_schedule(info, a->B, a->Hkv, G, splits, grid, &p.sched, &p.sched_stride);
@@ -1283,8 +1375,8 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
     p.part_dv = p.part_dk + static_cast<size_t>(splits) * part_rows * D;
   }
   cudaError_t e =
-      cap ? launch_kernel(dkv_kernel<D, true>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p)
-          : launch_kernel(dkv_kernel<D, false>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
+      cap ? launch_kernel(dkv_kernel<D, true>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, tdk, tdv, p)
+          : launch_kernel(dkv_kernel<D, false>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, tdk, tdv, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess && splits > 1) {
     const int64_t n4 = part_rows * D / 4;

@@ -41,4 +41,20 @@ inline bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
+// The same view copied in boxes of [box_rows, 32] (64-byte rows) with the
+// 64-byte swizzle: 16-byte chunk j of box row r sits at chunk j ^ ((r >> 1) & 3).
+inline bool make_tmap_bf16_2d_sw64(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                                   uint64_t row_bytes, uint32_t box_rows) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace bsa
