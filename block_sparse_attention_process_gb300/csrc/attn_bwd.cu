@@ -132,6 +132,36 @@ __device__ __forceinline__ void store_row(void* base, int fp32, int64_t row, int
   }
 }
 
+// store_row with 32-byte stores (half the store instructions of the
+// row-per-thread pattern) where the output is 32-byte aligned.
+__device__ __forceinline__ void store_row_wide(void* base, int fp32, int64_t row, int D, const uint32_t* v, int c0,
+                                               float mul) {
+  if ((reinterpret_cast<uintptr_t>(base) & 31u) != 0) {
+    store_row(base, fp32, row, D, v, c0, mul);
+    return;
+  }
+  if (fp32) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<float*>(base) + row * D + c0);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__uint_as_float(v[8 * e + i]) * mul);
+      st_global_v8(dst + 8 * e, w);
+    }
+  } else {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(base) + row * D + c0);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[i] = pack_bf16x2(__uint_as_float(v[16 * e + 2 * i]) * mul, __uint_as_float(v[16 * e + 2 * i + 1]) * mul);
+      st_global_v8(dst + 8 * e, w);
+    }
+  }
+}
+
 __device__ __forceinline__ void store_zero_cols(void* base, int fp32, int64_t row, int D, int c0, int n) {
   if (fp32) {
     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + row * D + c0);
@@ -447,7 +477,8 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (whole warp)
-    // order: S0 dP0 S1 | dQ0 dP1 S2 | dQ1 dP2 S3 | ...
+    // order: S0 dP0 S1 | dQ0 dP1 S2 | dQ1 dP2 S3 | ...; at a tile's last block
+    // L: ... dQ(L-1) dP(L) | dQ(L) S(L+1) dP(L+1) S(L+2) | ...
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
     constexpr uint64_t kTileDesc = kTile >> 4;
@@ -466,11 +497,16 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
     auto k_ready = [&](uint32_t n) -> bool {
       return mbar_wait_warp(&s.k_full[n % kDqStagesK], (n / kDqStagesK) & 1u, wc);
     };
-    auto issue_s = [&]() -> bool {  // S_n = Q K_n^T
+    // S_n = Q K_n^T.  A tile's first S waits until the previous tile's last
+    // dQ has been issued (allow_first false holds it back, s_cnt unchanged):
+    // that dQ, and so the epilogue, then never waits for the next tile's
+    // Q / dO load.
+    auto issue_s = [&](bool allow_first) -> bool {
       const uint32_t n = s_cnt;
       if (!k_ready(n)) return false;
       const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[n % kInfoRing].x, 0);
       if ((info >> 20) & 1u) {  // first block of a tile: wait for its Q/dO
+        if (!allow_first) return true;
         if (!mbar_wait_warp(&s.qo_full, q_uses & 1u, wc)) return false;
         ++q_uses;
       }
@@ -504,8 +540,8 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
       return true;
     };
     if (total > 0) {
-      ok = issue_s() && issue_dp();
-      if (ok && total > 1) ok = issue_s();
+      ok = issue_s(true) && issue_dp();
+      if (ok && total > 1) ok = issue_s(false);
     }
     for (uint32_t n = 0; ok && n < total; ++n) {
       const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[n % kInfoRing].x, 0);
@@ -525,8 +561,10 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
         mma_commit_elect(&s.acc_full);
         ++acc_uses;
       }
+      // a first S held back behind this dQ goes ahead of dP(n + 1)
+      if (s_cnt == n + 1 && s_cnt < total && !issue_s(true)) { ok = false; break; }
       if (dp_cnt < total && !issue_dp()) { ok = false; break; }
-      if (s_cnt < total && !issue_s()) { ok = false; break; }
+      if (s_cnt < total && !issue_s(false)) { ok = false; break; }
     }
     mma_commit_elect(&s.drain);
     uint32_t dummy_abort = 0;
@@ -647,7 +685,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
         tmem_ld32(tmem + kDqColQ + part * kPartD + c * 32 + lane_off, v);
         tmem_wait_ld();
         reg_fence32(v);
-        store_row(p.dq, p.grad_fp32, qrow, D, v, part * kPartD + c * 32, p.scale);
+        store_row_wide(p.dq, p.grad_fp32, qrow, D, v, part * kPartD + c * 32, p.scale);
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty);
