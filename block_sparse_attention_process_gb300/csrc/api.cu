@@ -296,13 +296,17 @@ bsa_status bsa_mask_info_view(const bsa_mask_info* info, bsa_mask_info_desc* out
 
 bsa_status bsa_mask_info_destroy(bsa_mask_info* info) {
   if (!info) return BSA_OK;
+  // no launch may still read the arrays; they go back to the library's
+  // stream-ordered pool they came from
   cudaDeviceSynchronize();
   void* ptrs[] = {info->block_mask, info->data_next, info->mask_next, info->partial,
                   info->q_sequence, info->row_len,   info->row_order};
   for (void* p : ptrs)
-    if (p) cudaFree(p);
-  for (auto& sc : info->schedules)
-    if (sc.dev) cudaFree(sc.dev);
+    if (p) pool_free(p, nullptr);
+  for (auto& sc : info->schedules) {
+    if (sc.dev) pool_free(sc.dev, nullptr);
+    if (sc.ready) cudaEventDestroy(sc.ready);
+  }
   delete info;
   return BSA_OK;
 }

@@ -1402,7 +1402,7 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
   }
   const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(p.n_tiles) * splits, num_sms()));
   if (schedule) {
-    bsa_status st = tile_schedule(info, a->B, a->Hkv, G, splits, grid, &p.sched, &p.sched_stride);
+    bsa_status st = tile_schedule(info, a->B, a->Hkv, G, splits, grid, stream, &p.sched, &p.sched_stride);
     if (st != BSA_OK) return st;
   }
   void* ws = nullptr;
@@ -1450,7 +1450,7 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
   }
   const int grid = std::min(p.n_tiles, num_sms());
   if (schedule) {
-    bsa_status st = tile_schedule(info, a->B, a->Hq, 1, 1, grid, &p.sched, &p.sched_stride);
+    bsa_status st = tile_schedule(info, a->B, a->Hq, 1, 1, grid, stream, &p.sched, &p.sched_stride);
     if (st != BSA_OK) return st;
   }
   cudaError_t e =

@@ -824,7 +824,7 @@ bsa_status launch_fwd(const FwdCall& c, const bsa_mask_info* info, float scale, 
     attr_set[xform] = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
-  bsa_status st = tile_schedule(info, c.B, c.Hq, 1, 1, grid, &p.sched, &p.sched_stride);
+  bsa_status st = tile_schedule(info, c.B, c.Hq, 1, 1, grid, stream, &p.sched, &p.sched_stride);
   if (st != BSA_OK) return st;
   cudaError_t e = xform ? launch_kernel(fwd_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, to, p)
                         : launch_kernel(fwd_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, to, p);

@@ -27,10 +27,15 @@ struct bsa_mask_info {
   int32_t* row_order = nullptr;      // [heads * rows] rows sorted by decreasing row_len (internal)
   // host copies of row_len / row_order, for the launch-time tile schedules
   std::vector<int32_t> row_len_h, row_order_h;
-  // tile schedules built so far (device memory, freed with the handle)
+  // tile schedules built so far (device memory from the library's pool,
+  // freed with the handle).  The upload is stream-ordered on the launch
+  // that built it; `ready` marks its end for launches on other streams, and
+  // `host` keeps the source alive.
   struct Schedule {
     int32_t n_b = 0, n_g = 0, group = 0, splits = 0, grid = 0, device = -1, stride = 0;
     int4* dev = nullptr;
+    cudaEvent_t ready = nullptr;
+    std::vector<int4> host;
   };
   mutable std::vector<Schedule> schedules;
   mutable std::mutex sched_mu;
@@ -74,9 +79,10 @@ int num_sms();
 // c's tiles are entries [c * stride, c * stride + stride) of *out, in
 // order, each {i, blocks, b * n_g + g, split}, ended early by blocks = -1.
 // Built on the first launch of a (n_b, n_g, group, splits, grid, device)
-// and cached in the MaskInfo.
+// and cached in the MaskInfo; `stream` (the launch's) is ordered after its
+// upload.
 bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t splits,
-                         int32_t grid, const int4** out, int32_t* stride);
+                         int32_t grid, cudaStream_t stream, const int4** out, int32_t* stride);
 
 // Stream-ordered device memory from the library's pool on the current
 // device (kept cached by the pool between calls).

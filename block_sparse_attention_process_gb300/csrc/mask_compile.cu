@@ -421,10 +421,14 @@ int idx_bytes(int64_t max_value) {
   return 4;
 }
 
+// Scratch memory of one compile, from the library's stream-ordered pool
+// (no device-wide synchronisation on release, unlike cudaFree).
 struct DevBuf {
+  cudaStream_t s;
   void* p = nullptr;
+  explicit DevBuf(cudaStream_t st) : s(st) {}
   ~DevBuf() {
-    if (p) cudaFree(p);
+    if (p) pool_free(p, s);
   }
 };
 
@@ -450,16 +454,27 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   if (n_cells > (int64_t(1) << 30)) return fail(BSA_ERR_UNSUPPORTED, "block grid too large");
   const bool dense = p.kind == BSA_MASK_DENSE;
 
-  DevBuf labels, hashes, stats, list, rep, new_id, slot_of_cell, hist;
+  DevBuf labels(stream), hashes(stream), stats(stream), list(stream), rep(stream), new_id(stream),
+      slot_of_cell(stream), hist(stream);
   cudaError_t e;
 #define BSA_CK(x, what)                         \
   do {                                          \
     e = (x);                                    \
     if (e != cudaSuccess) return cuda_fail(e, what); \
   } while (0)
+  // all device memory of a compile, scratch and MaskInfo arrays alike, comes
+  // from the stream-ordered pool; the final stream synchronisation makes the
+  // arrays usable from any stream
+#define BSA_ALLOC(ptr, bytes)                                          \
+  do {                                                                 \
+    void* q_ = nullptr;                                                \
+    const bsa_status s_ = pool_alloc(&q_, (bytes), stream);            \
+    if (s_ != BSA_OK) return s_;                                       \
+    (ptr) = static_cast<decltype(ptr)>(q_);                            \
+  } while (0)
 
-  BSA_CK(cudaMalloc(&labels.p, n_cells), "alloc labels");
-  BSA_CK(cudaMalloc(&stats.p, sizeof(Stats)), "alloc stats");
+  BSA_ALLOC(labels.p, n_cells);
+  BSA_ALLOC(stats.p, sizeof(Stats));
   BSA_CK(cudaMemsetAsync(stats.p, 0, sizeof(Stats), stream), "clear stats");
 
   auto* info = new bsa_mask_info();
@@ -481,14 +496,14 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   info->local_left = p.left;
   info->local_right = p.right;
   info->chunk = p.chunk;
-  BSA_CK(cudaMalloc(&info->row_len, n_rows * sizeof(int32_t)), "alloc row_len");
-  BSA_CK(cudaMalloc(&info->row_order, n_rows * sizeof(int32_t)), "alloc row_order");
-  BSA_CK(cudaMalloc(&info->q_sequence, p.q_len * sizeof(int32_t)), "alloc q_sequence");
+  BSA_ALLOC(info->row_len, n_rows * sizeof(int32_t));
+  BSA_ALLOC(info->row_order, n_rows * sizeof(int32_t));
+  BSA_ALLOC(info->q_sequence, p.q_len * sizeof(int32_t));
 
   const int grid_cells = static_cast<int>(std::min<int64_t>(n_cells, 152 * 64));
   Stats* st = static_cast<Stats*>(stats.p);
   if (dense) {
-    BSA_CK(cudaMalloc(&hashes.p, n_cells * sizeof(uint64_t)), "alloc hashes");
+    BSA_ALLOC(hashes.p, n_cells * sizeof(uint64_t));
     classify_dense<<<grid_cells, 256, 0, stream>>>(p, static_cast<int8_t*>(labels.p),
                                                   static_cast<uint64_t*>(hashes.p), n_cells);
   } else {
@@ -499,7 +514,7 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
       static_cast<int8_t*>(labels.p), p.nC, n_rows, info->row_len, st);
   BSA_CK(cudaGetLastError(), "row_pass launch");
   if (dense) {
-    BSA_CK(cudaMalloc(&list.p, n_cells * sizeof(int32_t)), "alloc list");
+    BSA_ALLOC(list.p, n_cells * sizeof(int32_t));
     compact_partial<<<1, 1024, 0, stream>>>(static_cast<int8_t*>(labels.p), n_cells,
                                             static_cast<int32_t*>(list.p), st);
     BSA_CK(cudaGetLastError(), "compact launch");
@@ -509,9 +524,9 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
 
   if (dense && hs.n1 > 0) {
-    BSA_CK(cudaMalloc(&rep.p, hs.n1 * sizeof(int32_t)), "alloc rep");
-    BSA_CK(cudaMalloc(&new_id.p, hs.n1 * sizeof(int32_t)), "alloc new_id");
-    BSA_CK(cudaMalloc(&slot_of_cell.p, n_cells * sizeof(int32_t)), "alloc slots");
+    BSA_ALLOC(rep.p, hs.n1 * sizeof(int32_t));
+    BSA_ALLOC(new_id.p, hs.n1 * sizeof(int32_t));
+    BSA_ALLOC(slot_of_cell.p, n_cells * sizeof(int32_t));
     const int warps_per_cta = 8;
     const int ctas = static_cast<int>(std::min<int64_t>((hs.n1 + warps_per_cta - 1) / warps_per_cta, 152 * 16));
     find_first_equal<<<ctas, 32 * warps_per_cta, 0, stream>>>(p, static_cast<int32_t*>(list.p), hs.n1,
@@ -527,13 +542,13 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
     BSA_CK(cudaGetLastError(), "scatter launch");
     BSA_CK(cudaMemcpyAsync(&hs.P, &st->P, sizeof(int32_t), cudaMemcpyDeviceToHost, stream), "read P");
     BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
-    BSA_CK(cudaMalloc(&info->partial, static_cast<size_t>(hs.P) * B * B), "alloc partial blocks");
+    BSA_ALLOC(info->partial, static_cast<size_t>(hs.P) * B * B);
     copy_stack<<<static_cast<unsigned>(std::min<int64_t>(hs.n1, 152 * 16)), 256, 0, stream>>>(
         p, static_cast<int32_t*>(list.p), static_cast<int32_t*>(new_id.p), hs.n1, info->partial);
     BSA_CK(cudaGetLastError(), "stack copy launch");
   } else if (dense) {
     hs.P = 0;
-    BSA_CK(cudaMalloc(&info->partial, 16), "alloc partial blocks");
+    BSA_ALLOC(info->partial, 16);
   }
 
   const int32_t width = opts->shrink ? hs.width : p.nC;
@@ -546,11 +561,11 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   info->mask_next_bytes = dense ? idx_bytes(hs.P > 0 ? hs.P - 1 : 0) : 0;
   const size_t n_out = static_cast<size_t>(n_rows) * width;
   const size_t alloc_n = n_out ? n_out : 1;
-  BSA_CK(cudaMalloc(&info->block_mask, alloc_n), "alloc block_mask");
-  BSA_CK(cudaMalloc(&info->data_next, alloc_n * info->data_next_bytes), "alloc data_next");
-  if (dense) BSA_CK(cudaMalloc(&info->mask_next, alloc_n * info->mask_next_bytes), "alloc mask_next");
+  BSA_ALLOC(info->block_mask, alloc_n);
+  BSA_ALLOC(info->data_next, alloc_n * info->data_next_bytes);
+  if (dense) BSA_ALLOC(info->mask_next, alloc_n * info->mask_next_bytes);
   if (dense && !slot_of_cell.p) {
-    BSA_CK(cudaMalloc(&slot_of_cell.p, n_cells * sizeof(int32_t)), "alloc slots");
+    BSA_ALLOC(slot_of_cell.p, n_cells * sizeof(int32_t));
     BSA_CK(cudaMemsetAsync(slot_of_cell.p, 0, n_cells * sizeof(int32_t), stream), "clear slots");
   }
   if (n_out) {
@@ -561,17 +576,23 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   }
   iota_i32<<<static_cast<unsigned>((p.q_len + 255) / 256), 256, 0, stream>>>(info->q_sequence, p.q_len);
   BSA_CK(cudaGetLastError(), "iota launch");
-  BSA_CK(cudaMalloc(&hist.p, (p.nC + 1) * sizeof(int32_t)), "alloc hist");
+  BSA_ALLOC(hist.p, (p.nC + 1) * sizeof(int32_t));
   order_rows<<<1, 1024, 0, stream>>>(info->row_len, static_cast<int32_t>(n_rows), p.nC,
                                      static_cast<int32_t*>(hist.p), info->row_order);
   BSA_CK(cudaGetLastError(), "order_rows launch");
-  BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
+  // host copies of the row lengths and order (for launch-time tile
+  // schedules), in stream order, then one synchronisation: a returned
+  // MaskInfo is complete
   info->row_len_h.resize(static_cast<size_t>(n_rows));
   info->row_order_h.resize(static_cast<size_t>(n_rows));
-  BSA_CK(cudaMemcpy(info->row_len_h.data(), info->row_len, n_rows * sizeof(int32_t), cudaMemcpyDeviceToHost),
+  BSA_CK(cudaMemcpyAsync(info->row_len_h.data(), info->row_len, n_rows * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                         stream),
          "copy row_len");
-  BSA_CK(cudaMemcpy(info->row_order_h.data(), info->row_order, n_rows * sizeof(int32_t), cudaMemcpyDeviceToHost),
+  BSA_CK(cudaMemcpyAsync(info->row_order_h.data(), info->row_order, n_rows * sizeof(int32_t),
+                         cudaMemcpyDeviceToHost, stream),
          "copy row_order");
+  BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
+#undef BSA_ALLOC
 #undef BSA_CK
   guard.keep = true;
   *out = info;

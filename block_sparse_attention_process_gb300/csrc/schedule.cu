@@ -16,7 +16,7 @@
 namespace bsa {
 
 bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t splits,
-                         int32_t grid, const int4** out, int32_t* stride) {
+                         int32_t grid, cudaStream_t stream, const int4** out, int32_t* stride) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -24,6 +24,8 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
   for (const auto& sc : info->schedules)
     if (sc.n_b == n_b && sc.n_g == n_g && sc.group == group && sc.splits == splits && sc.grid == grid &&
         sc.device == dev) {
+      e = cudaStreamWaitEvent(stream, sc.ready, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "wait for the tile schedule upload");
       *out = sc.dev;
       *stride = sc.stride;
       return BSA_OK;
@@ -79,15 +81,22 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
   for (int32_t c = 0; c < grid; ++c)
     std::copy(lists[static_cast<size_t>(c)].begin(), lists[static_cast<size_t>(c)].end(),
               flat.begin() + static_cast<size_t>(c) * st);
-  int4* d = nullptr;
-  e = cudaMalloc(&d, flat.size() * sizeof(int4));
-  if (e != cudaSuccess) return cuda_fail(e, "alloc tile schedule");
-  e = cudaMemcpy(d, flat.data(), flat.size() * sizeof(int4), cudaMemcpyHostToDevice);
+  // stream-ordered upload (no synchronisation with earlier work on the
+  // device), from a host copy that lives as long as the schedule
+  bsa_mask_info::Schedule sc;
+  sc.host = std::move(flat);
+  void* dv = nullptr;
+  bsa_status bs = pool_alloc(&dv, sc.host.size() * sizeof(int4), stream);
+  if (bs != BSA_OK) return bs;
+  int4* d = static_cast<int4*>(dv);
+  e = cudaMemcpyAsync(d, sc.host.data(), sc.host.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sc.ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventRecord(sc.ready, stream);
   if (e != cudaSuccess) {
-    cudaFree(d);
+    if (sc.ready) cudaEventDestroy(sc.ready);
+    pool_free(d, stream);
     return cuda_fail(e, "upload tile schedule");
   }
-  bsa_mask_info::Schedule sc;
   sc.n_b = n_b;
   sc.n_g = n_g;
   sc.group = group;
@@ -96,7 +105,7 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
   sc.device = dev;
   sc.stride = st;
   sc.dev = d;
-  info->schedules.push_back(sc);
+  info->schedules.push_back(std::move(sc));
   *out = d;
   *stride = st;
   return BSA_OK;
