@@ -185,7 +185,8 @@ __device__ __forceinline__ uint32_t part_a_col(int kk) {
 template <int N>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
   if constexpr (N == 32) tmem_st32(taddr, r);
-  else tmem_st16(taddr, r);
+  else if constexpr (N == 16) tmem_st16(taddr, r);
+  else tmem_st8(taddr, r);
 }
 
 // Visibility bits of N (32 or 64) consecutive columns of one row of a stacked block.
@@ -724,7 +725,9 @@ struct __align__(1024) DkvSmem {
   // elementwise warp (at a tile's last item, once its tensor stores out of
   // the item's Q / dO buffers have read them; otherwise from the MMA warp)
   uint64_t in_full[kDkvStages], in_empty[kDkvStages];
-  uint64_t st_full, dpt_full, p_full, ds_full;
+  // p_full[h]: half h of every thread's query columns of P^T is in tensor
+  // memory (dV takes those k-steps first)
+  uint64_t st_full, dpt_full, p_full[2], ds_full;
   uint64_t acc_full, acc_empty, drain;
   // per item: {col | label<<16 | first<<20 | last<<21, stack slot (dense) or q_sequence of the
   // query block's first row (computable), 128*j = first key of the tile, row of that key in dK/dV}
@@ -873,7 +876,8 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     }
     mbar_init(&s.st_full, 1);
     mbar_init(&s.dpt_full, 1);
-    mbar_init(&s.p_full, 128 * DkvShape<D>::kParts);
+    mbar_init(&s.p_full[0], 128 * DkvShape<D>::kParts);
+    mbar_init(&s.p_full[1], 128 * DkvShape<D>::kParts);
     mbar_init(&s.ds_full, 128 * DkvShape<D>::kParts);
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, 128 * DkvShape<D>::kParts);
@@ -1044,16 +1048,31 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       const uint32_t fl = (flags >> (2u * (n & 7u))) & 3u;
       const bool first = fl & 1u, last = fl & 2u;
       const bool more = n + 1 < total;
-      // dV += P^T dO
-      if (!mbar_wait_warp(&s.p_full, n & 1u, wc)) { ok = false; break; }
+      // dV += P^T dO, the k-steps of each half of the parts' columns as
+      // soon as that half of P^T is in tensor memory
+      if (!mbar_wait_warp(&s.p_full[0], n & 1u, wc)) { ok = false; break; }
       if (first && acc_uses > 0 && !mbar_wait_warp(&s.acc_empty, (acc_uses - 1) & 1u, wc)) { ok = false; break; }
       tc_fence_after();
       const uint64_t domn = domn0 + st * kTileDesc;
+      {
+        constexpr int kSteps = DkvShape<D>::kCols / 16;  // k-steps per part
+        bool half_ok = true;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts_elect(tmem + kDkvColDV, tmem + kDkvColST + part_a_col<DkvShape<D>::kCols>(kk),
-                     domn + static_cast<uint64_t>(kk * 2048 >> 4),
-                     idesc_acc, (first && kk == 0) ? 0u : 1u);
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1) {
+            half_ok = mbar_wait_warp(&s.p_full[1], n & 1u, wc);
+            if (!half_ok) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            if ((kk % kSteps) / (kSteps / 2) != h) continue;
+            mma_ts_elect(tmem + kDkvColDV, tmem + kDkvColST + part_a_col<DkvShape<D>::kCols>(kk),
+                         domn + static_cast<uint64_t>(kk * 2048 >> 4), idesc_acc, (first && kk == 0) ? 0u : 1u);
+          }
+        }
+        if (!half_ok) { ok = false; break; }
+      }
       // next item's S^T over the P^T columns the dV MMA has just read
       if (more && !last) {
         if (!item_flags(n + 1)) { ok = false; break; }
@@ -1151,31 +1170,42 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       // P = exp2((s*scale - LSE) * log2e): (LSE - s*scale) then times -log2e, packed pairs
       float pv[kCols];
       if constexpr (!kCap) {
+        // two halves of the columns, each published as soon as it is in
+        // tensor memory so that dV starts on it
 #pragma unroll
-        for (int c4 = 0; c4 < kCols / 4; ++c4) {
-          const float4 l4 = lse4[c4];
-          const int c = c4 * 4;
-          float e0, e1, e2, e3;
-          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nsc2, f2_pack(l4.x, l4.y)),
-                           nl2e2),
-                    e0, e1);
-          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), nsc2, f2_pack(l4.z, l4.w)),
-                           nl2e2),
-                    e2, e3);
-          pv[c] = ex2_approx(e0);
-          pv[c + 1] = ex2_approx(e1);
-          pv[c + 2] = ex2_approx(e2);
-          pv[c + 3] = ex2_approx(e3);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c4 = h * kCols / 8; c4 < (h + 1) * kCols / 8; ++c4) {
+            const float4 l4 = lse4[c4];
+            const int c = c4 * 4;
+            float e0, e1, e2, e3;
+            f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nsc2,
+                                    f2_pack(l4.x, l4.y)),
+                             nl2e2),
+                      e0, e1);
+            f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), nsc2,
+                                    f2_pack(l4.z, l4.w)),
+                             nl2e2),
+                      e2, e3);
+            pv[c] = ex2_approx(e0);
+            pv[c + 1] = ex2_approx(e1);
+            pv[c + 2] = ex2_approx(e2);
+            pv[c + 3] = ex2_approx(e3);
+          }
+          if (label == 1) {
+#pragma unroll
+            for (int c = h * kCols / 2; c < (h + 1) * kCols / 2; ++c)
+              if (!((allowed >> c) & 1ull)) pv[c] = 0.f;
+          }
+          uint32_t ppk[kCols / 4];
+#pragma unroll
+          for (int c = 0; c < kCols / 4; ++c)
+            ppk[c] = pack_bf16x2(pv[h * kCols / 2 + 2 * c], pv[h * kCols / 2 + 2 * c + 1]);
+          tmem_st_cols<kCols / 4>(tmem + kDkvColST + col0 + h * (kCols / 4) + lane_off, ppk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&s.p_full[h]);
         }
-        if (label == 1) {
-#pragma unroll
-          for (int c = 0; c < kCols; ++c)
-            if (!((allowed >> c) & 1ull)) pv[c] = 0.f;
-        }
-        uint32_t ppk[kCols / 2];
-#pragma unroll
-        for (int c = 0; c < kCols / 2; ++c) ppk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-        tmem_st_cols<kCols / 2>(tmem + kDkvColST + col0 + lane_off, ppk);
       } else {
         // soft cap: P = exp2(cap_log2 * t - LSE * log2e), t = tanh(s * cap_scale);
         // P^T goes to tensor memory for dV, and pv keeps P (1 - t^2) for dS
@@ -1195,10 +1225,11 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           pv[c + 1] = p1 * fmaf(-t1, t1, 1.f);
         }
         tmem_st_cols<kCols / 2>(tmem + kDkvColST + col0 + lane_off, ppk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&s.p_full[0]);
+        mbar_arrive(&s.p_full[1]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&s.p_full);
       if (!mbar_wait_warp(&s.dpt_full, n & 1u, wc)) { ok = false; break; }
       tc_fence_after();
       const float4* ds4 = reinterpret_cast<const float4*>(&s.dsum[st][col0]);
