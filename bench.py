@@ -79,6 +79,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over the ranks of the default process group (x itself
+    when there is none or it has one rank)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_rank: float, seconds: float, world: int) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return world * flop_per_rank / seconds / 1e12
+
+
 def mask_kwargs(w):
     if w.mask.kind == "local":
         return {"local_left": w.mask.left, "local_right": w.mask.right}
@@ -246,11 +262,8 @@ def run_gpu(args):
         per["dq"].append(e[3].elapsed_time(e[4]))
         per["step"].append(e[0].elapsed_time(e[4]))
     ms = {k: sum(v) / len(v) for k, v in per.items()}
-    if ws > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = ws * (f_fwd + f_bwd) / (step_ms * 1e-3) / 1e12
+    step_ms = max_over_ranks(step_ms, dev)
+    value = job_tflops(f_fwd + f_bwd, step_ms * 1e-3, ws)
 
     # per-kernel algorithmic work: executed GEMMs of 2*128*128*D FLOP per block and q head
     gemm = n_exec * w.B * w.Hq * 2 * 128 * 128 * w.D
@@ -361,12 +374,8 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws):
     t0 = time.perf_counter()
     for _ in range(n):
         one()
-    dt = (time.perf_counter() - t0) / n
-    if ws > 1:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
-    return {"value": round(ws * total_flop / dt / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(dt * 1e3, 3),
+    dt = max_over_ranks((time.perf_counter() - t0) / n, dev)
+    return {"value": round(job_tflops(total_flop, dt, ws), 2), "unit": "TFLOP/s", "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "includes": "mask compile (fwd+dkv), H2D Q/K/V and dO (dO on a side stream during the forward), fwd, "
                         "rowsum, dK/dV, dQ, D2H dK/dV (side stream, during dQ) and dQ"}
