@@ -127,6 +127,28 @@ def test_repeat_run_is_deterministic():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_maskinfo_shared_by_two_streams():
+    """A MaskInfo's launch-time tile schedule is uploaded in stream order on
+    the first launch's stream; a launch on another stream waits for that
+    upload and gives the same result."""
+    need_gpu()
+    import block_sparse_attention_process_gb300 as bsa
+    q, k, v, _ = qkvdo(1, 4, 2, 1024, 128, seed=9, with_do=False)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    info = bsa.mask_compile("causal", 1024, 1024)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s1):
+        o1, l1 = bsa.fwd(q, k, v, info)
+    with torch.cuda.stream(s2):
+        o2, l2 = bsa.fwd(q, k, v, info)
+    torch.cuda.synchronize()
+    assert bsa.get_device_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ro, rl = oatt.forward(f64(q), f64(k), f64(v), {"kind": "causal", "kv_len": 1024})
+    compare("O", o2.float().cpu().numpy(), ro, TOL_O)
+    compare("LSE", l2.cpu().numpy(), rl, TOL_LSE)
+
+
 # ---------------------------------------------------------------- full size
 
 def sampled_rows(S, n, rng):
