@@ -23,7 +23,8 @@ import torch
 from . import _abi
 from ._abi import BsaError, check
 
-__all__ = ["mask_compile", "MaskInfo", "fwd", "bwd", "bwd_noalloc", "bwd_rowsum", "bwd_dkv", "bwd_dq",
+__all__ = ["mask_compile", "MaskInfo", "fwd", "fwd_partial", "fwd_merge", "bwd", "bwd_noalloc", "bwd_rowsum",
+           "bwd_dkv", "bwd_dq",
            "get_device_error", "set_wait_limit_ns", "debug_wait_timeout", "version", "BsaError",
            "library_path"]
 
