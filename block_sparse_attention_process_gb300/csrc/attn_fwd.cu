@@ -43,7 +43,7 @@ namespace {
 
 constexpr int kStagesK = 2;
 constexpr int kStagesV = 2;
-constexpr int kSBufs = 3;         // score buffers in TMEM
+constexpr int kSBufs = 2;         // score buffers in TMEM
 constexpr int kInfoRing = 32;     // block descriptors published by the walker warp
 // The softmax is split over kParts warpgroups, each taking kCols of the 128
 // score columns of every row (and D / kParts of the O columns).
@@ -62,7 +62,10 @@ constexpr uint32_t kFirst = 1u << 20;  // first block of its tile
 constexpr uint32_t kLast = 1u << 21;   // last block of its tile
 constexpr uint32_t kEnd = 1u << 22;    // no more blocks for this CTA
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 384;  // O accumulator after three 128-column score buffers
+// One O accumulator per softmax part after the two 128-column score
+// buffers: part p's running maximum is its own, so its P V goes to its own
+// accumulator, and the epilogue combines the parts.
+constexpr uint32_t kTmemO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by more
 
 template <int D>
@@ -84,10 +87,9 @@ struct __align__(1024) FwdSmem {
   // (b*Hq + hq)*Sq + 128*i = Q and output row of the tile's first query}
   uint4 binfo[kInfoRing];
   uint32_t bkrow[kInfoRing];  // K/V row of the block's first key
-  float xmax[2][kParts][128];  // partial row maxima per [block parity][part][row]
   // a finished tile's row statistics for the epilogue warpgroup, per [tile
-  // parity]: the row maximum (log2 units) and each part's partial row sum
-  float tmax[2][128];
+  // parity][part]: the part's running maximum (log2 units) and row sum
+  float tmax[2][kParts][128];
   float tsum[2][kParts][128];
   uint32_t trow[2];              // output row of the tile's first query
   uint64_t stats_full[2], stats_empty[2];
@@ -426,10 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(&s.v_full[vs], (pv_cnt / kStagesV) & 1u, wc)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = vdesc0 + vs * kTileDesc;
+      // part p's P (keys [64p, 64p + 64), words [64p, 64p + 32) of the
+      // buffer) into part p's accumulator
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_elect(tmem + kTmemO, tmem + pb * 128 + kk * 8, vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_o,
-                     (pv_first && kk == 0) ? 0u : 1u);
+        mma_ts_elect(tmem + kTmemO + (kk >> 2) * 128, tmem + pb * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+                     vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_o, (pv_first && (kk & 3) == 0) ? 0u : 1u);
       mma_commit_elect(&s.v_empty[vs]);
       mma_commit_elect(&s.pv_done[pb]);
       if (pv_last) {
@@ -448,8 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue warpgroup
     // One query row per thread: waits for a tile's statistics and its final
-    // O, reads O out of tensor memory (then releases it for the next tile's
-    // P V) and writes O / l in bf16 and the logsumexp.
+    // accumulators, combines the parts' (maximum m_p, sum l_p, O_p) with the
+    // weights w_p = 2^(m_p - M), M = max over the parts with l_p > 0:
+    // O = sum w_p O_p / L, L = sum w_p l_p; reads O out of tensor memory
+    // (then releases it for the next tile's P V) and writes O in bf16 and the
+    // logsumexp M + log2 L (natural-log units).
     const int quarter = warp - kEpiWarp0;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -461,26 +468,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(&s.stats_full[tp], (t >> 1) & 1u, wc)) { ok = false; break; }
       const uint32_t row0 = s.trow[tp];
       if (row0 == 0xFFFFFFFFu) break;  // end mark from the softmax warps
-      const float mrow = s.tmax[tp][r];
-      float l_row = 0.f;
-#pragma unroll
-      for (int q = 0; q < kParts; ++q) l_row += s.tsum[tp][q][r];
+      static_assert(kParts == 2, "the epilogue combines two parts");
+      const float m0 = s.tmax[tp][0][r], m1 = s.tmax[tp][1][r];
+      const float l0 = s.tsum[tp][0][r], l1 = s.tsum[tp][1][r];
       mbar_arrive(&s.stats_empty[tp]);
+      const float mrow = fmaxf(l0 > 0.f ? m0 : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
+      const float w0 = l0 > 0.f ? ex2_approx(m0 - mrow) : 0.f;
+      const float w1 = l1 > 0.f ? ex2_approx(m1 - mrow) : 0.f;
+      const float l_row = l0 * w0 + l1 * w1;
       if (!mbar_wait_warp(&s.o_full, t & 1u, wc)) { ok = false; break; }
       tc_fence_after();
       const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
+      // per-part factors of the output: normalised (bf16 O) or not (a shard's accumulator)
+      const float c0 = p.partial ? w0 : w0 * inv_l, c1 = p.partial ? w1 : w1 * inv_l;
       const int64_t orow = static_cast<int64_t>(row0) + r;
       if (p.partial) {
-        // (a key shard) the unnormalised fp32 accumulator, 16 columns at a time
-        uint4* dst = reinterpret_cast<uint4*>(p.o_acc + orow * D);
+        // (a key shard) the unnormalised fp32 accumulator w0 O_0 + w1 O_1 (for
+        // the reference maximum M), 16 columns at a time
+        float4* dst = reinterpret_cast<float4*>(p.o_acc + orow * D);
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
-          uint32_t va[16];
+          uint32_t va[16], vb[16];
           tmem_ld16(obase + c * 16, va);
+          tmem_ld16(obase + 128 + c * 16, vb);
           tmem_wait_ld();
           reg_fence16(va);
+          reg_fence16(vb);
+          float o[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[c * 4 + e] = make_uint4(va[4 * e], va[4 * e + 1], va[4 * e + 2], va[4 * e + 3]);
+          for (int j = 0; j < 16; ++j) o[j] = fmaf(__uint_as_float(va[j]), c0, __uint_as_float(vb[j]) * c1);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[c * 4 + e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
         }
         // (every load of this tile's O has completed by the last wait)
         tc_fence_before();
@@ -498,13 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            uint32_t va[16];
+            uint32_t va[16], vb[16];
             tmem_ld16(obase + h * 64 + c * 16, va);
+            tmem_ld16(obase + 128 + h * 64 + c * 16, vb);
             tmem_wait_ld();
             reg_fence16(va);
+            reg_fence16(vb);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              pk[c * 8 + j] = pack_bf16x2(__uint_as_float(va[2 * j]) * inv_l, __uint_as_float(va[2 * j + 1]) * inv_l);
+              pk[c * 8 + j] = pack_bf16x2(fmaf(__uint_as_float(va[2 * j]), c0, __uint_as_float(vb[2 * j]) * c1),
+                                          fmaf(__uint_as_float(va[2 * j + 1]), c0, __uint_as_float(vb[2 * j + 1]) * c1));
           }
           if (h == D / 64 - 1) {
             tc_fence_before();
@@ -537,21 +558,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax (kParts warpgroups)
     // Warpgroup `part` takes score columns [kCols*part, kCols*part + kCols)
-    // of every row; the warps with the same lanes (rows) in the kParts
-    // warpgroups exchange their partial row maxima through shared memory.
-    constexpr int kOCols = D / kParts;  // O columns per part
+    // of every row with a running maximum and sum of its own (no exchange
+    // between the parts); its P V goes to its own O accumulator, and the
+    // epilogue combines the parts' (maximum, sum, O).
     const int part = (warp - 4) >> 2;
     const int quarter = (warp - 4) & 3;
     const int r = quarter * 32 + lane;  // query row in the tile == TMEM lane
-    const uint32_t bar_id = 1u + static_cast<uint32_t>(quarter);
-    constexpr uint32_t kBarThreads = 32 * kParts;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t col0 = static_cast<uint32_t>(part) * kCols;  // first score column of this part
-    const uint32_t ocol0 = kTmemO + static_cast<uint32_t>(part) * kOCols;
+    const uint32_t ocol0 = kTmemO + static_cast<uint32_t>(part) * 128;  // this part's O accumulator
     const float scale_log2 = p.scale_log2;
     uint32_t n = 0;
     bool ok = true;
-    float m = -INFINITY, l = 0.f;  // l: this part's partial row sum
+    float m = -INFINITY, l = 0.f;  // this part's running maximum (log2 units) and row sum
     int64_t lo = 0, hi = 0;
     uint32_t exec = 0;
     uint32_t tiles = 0;
@@ -559,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto finish_tile = [&](uint32_t row) -> bool {
       const uint32_t tp = tiles & 1u;
       if (tiles >= 2 && !mbar_wait_warp(&s.stats_empty[tp], ((tiles >> 1) - 1) & 1u, wc)) return false;
-      if (part == 0) s.tmax[tp][r] = (m == -INFINITY) ? 0.f : m;
+      s.tmax[tp][part][r] = m;
       s.tsum[tp][part][r] = l;
       if (r == 0 && part == 0) s.trow[tp] = row;
       mbar_arrive(&s.stats_full[tp]);
@@ -585,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = 0.f;
         exec = 0;
         if (kX && p.n_sinks > 0) {
-          // the sinks open the row's running maximum and (in part 0) its sum
+          // the sinks open the running maximum of both parts and the sum of part 0
           const int32_t hq = static_cast<int32_t>((static_cast<int64_t>(bi.w) / p.Sq) % p.Hq);
           const float* z = p.sinks + (p.sinks_kv ? (hq / (p.Hq / p.Hkv)) * p.n_sinks : 0);
           for (int j = 0; j < p.n_sinks; ++j) m = fmaxf(m, z[j] * 1.4426950408889634f);
@@ -648,18 +667,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         m3 = fmax3(m3, __uint_as_float(xu[c + 6]), __uint_as_float(xu[c + 7]));
       }
       const float pm = fmax3(fmaxf(m0, m1), m2, m3);
-      // exchange with the other parts of the row (double-buffered by block parity)
-      s.xmax[n & 1u][part][r] = pm;
-      named_bar_sync(bar_id, kBarThreads);
-      float mx = s.xmax[n & 1u][0][r];
-#pragma unroll
-      for (int q = 1; q < kParts; ++q) mx = fmaxf(mx, s.xmax[n & 1u][q][r]);
+      const float mx = pm;
       // tanh is increasing: the capped maximum is the cap of the maximum
       const float m_blk = (!kX || p.cap_scale == 0.f) ? mx * scale_log2
                           : (mx == -INFINITY ? -INFINITY : p.cap_log2 * tanh_fast(mx * p.cap_scale));
       const float m_cand = fmaxf(m, m_blk);
       const bool switch_ref = m_cand > m + kRescaleThreshold;
-      const bool warp_switch = __any_sync(0xffffffffu, switch_ref);  // same rows, same values in every part
+      const bool warp_switch = __any_sync(0xffffffffu, switch_ref);
       float alpha = 1.f;
       if (warp_switch) {
         alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_cand);
@@ -700,21 +714,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rs0, rs1;
       f2_unpack(acc01, rs0, rs1);
       l = l * alpha + (rs0 + rs1);
-      // P (bf16 pairs) over the first 64 columns of the score buffer: this
-      // part's probabilities go to words [part*kCols/2, (part+1)*kCols/2);
-      // every part finished reading its scores before the exchange barrier.
+      // P (bf16 pairs) over the first half of this part's own score columns:
+      // words [part*kCols, part*kCols + kCols/2) of the buffer.
 #pragma unroll
       for (int c = 0; c < kCols / 2; c += 16)
-        tmem_st16(tmem + sb * 128 + static_cast<uint32_t>(part) * (kCols / 2) + c + lane_off, pk + c);
+        tmem_st16(tmem + sb * 128 + static_cast<uint32_t>(part) * kCols + c + lane_off, pk + c);
       // O holds earlier blocks' sum only after the first block; rescale this
-      // part's O columns (after the previous P V has landed) when the max moved.
+      // part's accumulator (after the previous P V has landed) when its max moved.
       if (warp_switch && exec > 0) {
         const uint32_t prev = n - 1;
         if (!mbar_wait_warp(&s.pv_done[prev % kSBufs], (prev / kSBufs) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
         const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
-        for (int c = 0; c < kOCols; c += 16) {
+        for (int c = 0; c < D; c += 16) {
           uint32_t ov[16];
           const uint32_t oa = tmem + ocol0 + c + lane_off;
           tmem_ld16(oa, ov);
