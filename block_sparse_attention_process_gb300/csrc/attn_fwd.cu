@@ -13,19 +13,22 @@
 // divide at the end.
 //
 // GB300 design (one persistent CTA per SM, warp-specialised):
-//   warp 0      TMA producer of Q tiles (2 buffers) and K blocks (3 stages)
+//   warp 0      TMA producer of Q tiles (2 buffers) and K blocks (2 stages)
 //   warp 1      tcgen05 issuer, warp-converged (one elected lane issues):
-//               S = Q K^T into one of three TMEM score buffers, up to three
-//               blocks ahead of the P V it is waiting for, and O += P V
-//               with P read from TMEM (bf16 over its score buffer)
+//               S = Q K^T into one of two TMEM score buffers, a block ahead
+//               of the softmax, and O_p += P_p V_p for each softmax part p,
+//               P_p read from TMEM (bf16 over the part's own score columns)
 //   warp 2      TMA producer of V blocks (2 stages)
-//   warps 4-11  softmax in two warpgroups, one (row, half of the columns)
-//               per thread: mask, row max (halves exchanged through shared
-//               memory), exp2, row sum, P to TMEM, lazy O rescale in TMEM;
-//               at a tile's end the row statistics go to shared memory and
-//               the softmax moves straight on to the next tile
-//   warps 12-15 epilogue: O / l from TMEM to bf16 in HBM and the
-//               logsumexp, one row per thread, while the next tile runs
+//   warp 3      walker: follows the CTA's tile list and the MaskInfo rows
+//               and publishes one descriptor per non-empty block
+//   warps 4-11  softmax in two warpgroups (parts), one (row, half of the
+//               columns) per thread, each part with its own running maximum
+//               and sum: mask, row max, exp2, row sum, P to TMEM, lazy
+//               rescale of the part's O in TMEM; at a tile's end the
+//               statistics go to shared memory and the softmax moves on
+//   warps 12-15 epilogue: combines the parts' (maximum, sum, O) into O / l
+//               in bf16 (tensor stores) and the logsumexp, one row per
+//               thread, while the next tile runs
 // Each CTA walks one fixed sequence of (tile, block) pairs; every role
 // walks it the same way, so the pipelines stay in step without sharing
 // state.  Work tiles are (batch, query head, query block), longest rows
