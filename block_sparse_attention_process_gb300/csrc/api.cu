@@ -300,7 +300,7 @@ bsa_status bsa_mask_info_destroy(bsa_mask_info* info) {
   // stream-ordered pool they came from
   cudaDeviceSynchronize();
   void* ptrs[] = {info->block_mask, info->data_next, info->mask_next, info->partial,
-                  info->q_sequence, info->row_len,   info->row_order};
+                  info->partial_bits, info->q_sequence, info->row_len, info->row_order};
   for (void* p : ptrs)
     if (p) pool_free(p, nullptr);
   for (auto& sc : info->schedules) {

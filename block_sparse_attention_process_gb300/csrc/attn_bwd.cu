@@ -191,18 +191,10 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) 
 
 // Visibility bits of N (32 or 64) consecutive columns of one row of a stacked block.
 template <int N>
-__device__ __forceinline__ uint64_t dense_bits(const uint8_t* row) {
-  uint64_t bits = 0;
-  const uint4* src = reinterpret_cast<const uint4*>(row);
-#pragma unroll
-  for (int v = 0; v < N / 16; ++v) {
-    const uint4 w = __ldg(src + v);
-    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-      if ((wv[e >> 2] >> ((e & 3) * 8)) & 0xFFu) bits |= 1ull << (v * 16 + e);
-  }
-  return bits;
+__device__ __forceinline__ uint64_t dense_bits(const uint32_t* row_bits, uint32_t c0) {
+  // row_bits: the block row's 4 words of visibility bits (c0 a multiple of N)
+  if constexpr (N == 64) return __ldg(reinterpret_cast<const unsigned long long*>(row_bits) + (c0 >> 6));
+  else return static_cast<uint64_t>(__ldg(row_bits + (c0 >> 5)));
 }
 
 // Bits of the columns [c0, c0+64) that lie inside [lo, hi].
@@ -347,7 +339,7 @@ struct DqSeq {
 };
 
 // kCap: the logit soft cap is compiled in (a separate instantiation).
-template <int D, bool kCap>
+template <int D, bool kCap, int kM>
 __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -607,7 +599,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
       if (first) {
         // row statistics arrive with the tile's Q/dO; q_sequence is consecutive within a block
         qrow = static_cast<int64_t>(bi.w) + r;
-        if (p.mi.kind != BSA_MASK_DENSE)
+        if (!dense_mask<kM>(p.mi.kind))
           key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(static_cast<int32_t>(bi.z)) + r,
                        lo, hi);
         if (!mbar_wait_warp(&s.qo_full, tiles & 1u, wc)) { ok = false; break; }
@@ -618,8 +610,8 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
       }
       uint64_t allowed = ~0ull;
       if (label == 1) {
-        if (p.mi.kind == BSA_MASK_DENSE)
-          allowed = dense_bits<kCols>(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
+        if (dense_mask<kM>(p.mi.kind))
+          allowed = dense_bits<kCols>(p.mi.partial_bits + (bi.y * 128u + static_cast<uint32_t>(r)) * 4u, col0);
         else
           allowed = interval_bits_64(static_cast<int64_t>(col) * 128 + col0, lo, hi);
       }
@@ -850,7 +842,7 @@ struct DkvItems {
 };
 
 // kCap: the logit soft cap is compiled in (a separate instantiation).
-template <int D, bool kCap>
+template <int D, bool kCap, int kM>
 __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -1145,14 +1137,14 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
         krow = static_cast<int64_t>(bi.w) + r;
-        if (p.mi.kind != BSA_MASK_DENSE)
+        if (!dense_mask<kM>(p.mi.kind))
           query_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(bi.z) + r, lo, hi);
       }
       if (!mbar_wait_warp(&s.st_full, n & 1u, wc)) { ok = false; break; }
       uint64_t allowed = ~0ull;
       if (label == 1) {
-        if (p.mi.kind == BSA_MASK_DENSE) {
-          allowed = dense_bits<kCols>(p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
+        if (dense_mask<kM>(p.mi.kind)) {
+          allowed = dense_bits<kCols>(p.mi.partial_bits + (bi.y * 128u + static_cast<uint32_t>(r)) * 4u, col0);
         } else {
           // q_sequence is consecutive within a query block
           allowed = interval_bits_64(static_cast<int64_t>(static_cast<int32_t>(bi.y)) + col0, lo, hi);
@@ -1396,13 +1388,17 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
   p.n_tiles = a->B * a->Hkv * p.nK;
   const bool cap = p.cap_scale != 0.f;
+  // instantiation: the soft cap (either mask kind), or none with the
+  // computable or the dense mask compiled in
+  const int variant = cap ? 2 : (info->kind == BSA_MASK_DENSE ? 1 : 0);
+  auto kern = variant == 2 ? dkv_kernel<D, true, kAnyMask>
+                           : (variant == 1 ? dkv_kernel<D, false, kDenseMask> : dkv_kernel<D, false, kComputableMask>);
   const size_t smem = sizeof(DkvSmem<D>) + 1024;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[cap]) {
-    cudaError_t e = cudaFuncSetAttribute(cap ? dkv_kernel<D, true> : dkv_kernel<D, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attr_set[3] = {false, false, false};
+  if (!attr_set[variant]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "set dkv smem size");
-    attr_set[cap] = true;
+    attr_set[variant] = true;
   }
   // With few KV tiles (MQA, short sequences) the q heads of a group are
   // split over several CTAs: the smallest divisor of the group that gives
@@ -1444,8 +1440,7 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
     p.part_dv = p.part_dk + static_cast<size_t>(splits) * part_rows * D;
   }
   cudaError_t e =
-      cap ? launch_kernel(dkv_kernel<D, true>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, tdk, tdv, p)
-          : launch_kernel(dkv_kernel<D, false>, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, tdk, tdv, p);
+      launch_kernel(kern, dim3(grid), dim3(DkvShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, tdk, tdv, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess && splits > 1) {
     const int64_t n4 = part_rows * D / 4;
@@ -1471,22 +1466,22 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
   p.n_tiles = a->B * a->Hq * p.nQ;
   const bool cap = p.cap_scale != 0.f;
+  const int variant = cap ? 2 : (info->kind == BSA_MASK_DENSE ? 1 : 0);
+  auto kern = variant == 2 ? dq_kernel<D, true, kAnyMask>
+                           : (variant == 1 ? dq_kernel<D, false, kDenseMask> : dq_kernel<D, false, kComputableMask>);
   const size_t smem = sizeof(DqSmem<D>) + 1024;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[cap]) {
-    cudaError_t e = cudaFuncSetAttribute(cap ? dq_kernel<D, true> : dq_kernel<D, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attr_set[3] = {false, false, false};
+  if (!attr_set[variant]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "set dq smem size");
-    attr_set[cap] = true;
+    attr_set[variant] = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
   if (schedule) {
     bsa_status st = tile_schedule(info, a->B, a->Hq, 1, 1, grid, stream, &p.sched, &p.sched_stride);
     if (st != BSA_OK) return st;
   }
-  cudaError_t e =
-      cap ? launch_kernel(dq_kernel<D, true>, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p)
-          : launch_kernel(dq_kernel<D, false>, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
+  cudaError_t e = launch_kernel(kern, dim3(grid), dim3(DqShape<D>::kThreads), smem, stream, tq, tk, tv, tdo, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dq launch");
   return BSA_OK;

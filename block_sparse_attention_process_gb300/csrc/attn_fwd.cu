@@ -132,8 +132,10 @@ struct FwdParams {
 };
 
 // kX: the logit soft cap and / or attention sinks are compiled in (a
-// separate instantiation, so that the plain kernel keeps its code).
-template <int D, bool kX>
+// separate instantiation, so that the plain kernel keeps its code); kBits:
+// a dense mask's partial blocks are read as bits (the instantiation for
+// dense masks without the transforms; the others read the bytes).
+template <int D, bool kX, bool kBits>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -621,7 +623,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint64_t mbits = ~0ull;  // visibility of this part's columns (label 1 only)
       if (label == 1) {
-        if (p.mi.kind == BSA_MASK_DENSE) {
+        if constexpr (kBits) {
+          // this part's 64 visibility bits of the stacked block's row
+          static_assert(kCols == 64, "one 64-bit word of mask bits per part");
+          mbits = __ldg(reinterpret_cast<const unsigned long long*>(p.mi.partial_bits +
+                                                                     (static_cast<int64_t>(bi.y) * 128 + r) * 4) +
+                        part);
+        } else if (p.mi.kind == BSA_MASK_DENSE) {
           const uint4* mrow = reinterpret_cast<const uint4*>(
               p.mi.partial + (static_cast<int64_t>(bi.y) * 128 + r) * 128 + col0);
           mbits = 0;
@@ -831,19 +839,21 @@ bsa_status launch_fwd(const FwdCall& c, const bsa_mask_info* info, float scale, 
   p.wait_ns = wait_limit_ns();
   if (!p.err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
   const bool xform = p.cap_scale != 0.f || p.n_sinks > 0;
+  // instantiation: the logit transforms, the dense mask read as bits, or neither
+  const int variant = xform ? 2 : (info->kind == BSA_MASK_DENSE ? 1 : 0);
+  auto kern = variant == 2 ? fwd_kernel<D, true, false>
+                           : (variant == 1 ? fwd_kernel<D, false, true> : fwd_kernel<D, false, false>);
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[xform]) {
-    cudaError_t e = cudaFuncSetAttribute(xform ? fwd_kernel<D, true> : fwd_kernel<D, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attr_set[3] = {false, false, false};
+  if (!attr_set[variant]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "set forward smem size");
-    attr_set[xform] = true;
+    attr_set[variant] = true;
   }
   const int grid = std::min(p.n_tiles, num_sms());
   bsa_status st = tile_schedule(info, c.B, c.Hq, 1, 1, grid, stream, &p.sched, &p.sched_stride);
   if (st != BSA_OK) return st;
-  cudaError_t e = xform ? launch_kernel(fwd_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, to, p)
-                        : launch_kernel(fwd_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, to, p);
+  cudaError_t e = launch_kernel(kern, dim3(grid), dim3(kThreads), smem, stream, tq, tk, tv, to, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return BSA_OK;

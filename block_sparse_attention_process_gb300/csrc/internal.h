@@ -22,6 +22,9 @@ struct bsa_mask_info {
   void* data_next = nullptr;         // [heads, rows, width]
   void* mask_next = nullptr;         // [heads, rows, width] or null
   uint8_t* partial = nullptr;        // [num_partial, 128, 128] or null
+  // the same blocks as bits (internal, for the kernels): word w of row r of
+  // block b, bit j = partial[b, r, 32 w + j]; [num_partial, 128, 4] or null
+  uint32_t* partial_bits = nullptr;
   int32_t* q_sequence = nullptr;     // [q_len]
   int32_t* row_len = nullptr;        // [heads, rows] non-empty blocks per row (internal)
   int32_t* row_order = nullptr;      // [heads * rows] rows sorted by decreasing row_len (internal)

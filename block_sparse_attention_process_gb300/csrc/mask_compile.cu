@@ -297,6 +297,22 @@ __global__ void scatter_slots(const int32_t* __restrict__ list, const int32_t* _
   slot_of_cell[list[k]] = new_id[rep[k]];
 }
 
+// The stacked blocks as bits for the attention kernels: one thread per
+// 32 columns of a row, bit j of the word = byte j of those columns.
+__global__ void __launch_bounds__(256) pack_stack_bits(const uint8_t* __restrict__ stack, int64_t n_words,
+                                                       uint32_t* __restrict__ bits) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_words;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(stack + i * 32);
+    const uint4 a = src[0], b = src[1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t out = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) out |= ((w[j >> 2] >> ((j & 3) * 8)) & 0xFFu) ? (1u << j) : 0u;
+    bits[i] = out;
+  }
+}
+
 // Copy each new partial block into its stack slot as 0/1 bytes (transposed
 // for the dkv orientation).  One CTA of 256 threads per list entry.
 __global__ void __launch_bounds__(256) copy_stack(MaskParams p, const int32_t* __restrict__ list,
@@ -546,9 +562,15 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
     copy_stack<<<static_cast<unsigned>(std::min<int64_t>(hs.n1, 152 * 16)), 256, 0, stream>>>(
         p, static_cast<int32_t*>(list.p), static_cast<int32_t*>(new_id.p), hs.n1, info->partial);
     BSA_CK(cudaGetLastError(), "stack copy launch");
+    const int64_t n_words = static_cast<int64_t>(hs.P) * B * (B / 32);
+    BSA_ALLOC(info->partial_bits, n_words * sizeof(uint32_t));
+    pack_stack_bits<<<static_cast<unsigned>(std::min<int64_t>((n_words + 255) / 256, 152 * 16)), 256, 0, stream>>>(
+        info->partial, n_words, info->partial_bits);
+    BSA_CK(cudaGetLastError(), "stack bits launch");
   } else if (dense) {
     hs.P = 0;
     BSA_ALLOC(info->partial, 16);
+    BSA_ALLOC(info->partial_bits, 16);
   }
 
   const int32_t width = opts->shrink ? hs.width : p.nC;

@@ -9,11 +9,23 @@
 
 namespace bsa {
 
+// The mask kind an attention kernel instantiation is compiled for: one whose
+// partial blocks are computed from each row's visible interval, one whose
+// partial blocks are read as bits from the stack, or either (decided at run
+// time; used by the instantiations with the logit transforms).
+enum MaskMode : int { kComputableMask = 0, kDenseMask = 1, kAnyMask = 2 };
+
+template <int kM>
+__device__ __forceinline__ bool dense_mask(int kind) {
+  return kM == kDenseMask || (kM == kAnyMask && kind == BSA_MASK_DENSE);
+}
+
 struct MaskInfoDev {
   const int8_t* block_mask;   // [heads, rows, width]
   const void* data_next;      // [heads, rows, width]
   const void* mask_next;      // [heads, rows, width] or null
   const uint8_t* partial;     // [P, 128, 128] or null
+  const uint32_t* partial_bits;  // [P, 128, 4]: bit j of word w = partial[., row, 32 w + j]
   const int32_t* q_sequence;  // [q_len]
   const int32_t* row_len;     // [heads, rows]
   const int32_t* row_order;   // [heads * rows]
@@ -30,6 +42,7 @@ inline MaskInfoDev mask_info_dev(const bsa_mask_info* info) {
   m.data_next = info->data_next;
   m.mask_next = info->mask_next;
   m.partial = info->partial;
+  m.partial_bits = info->partial_bits;
   m.q_sequence = info->q_sequence;
   m.row_len = info->row_len;
   m.row_order = info->row_order;
