@@ -125,12 +125,15 @@ typedef struct {
  * shrink pass and the integer downcast as kernels on `stream`, synchronising
  * `stream` to size the outputs and again before returning: the MaskInfo is
  * complete on return, and the attention kernels read it without waiting for
- * earlier work on their stream.  *out receives a new handle on success and
- * is untouched on failure. */
+ * earlier work on their stream.  Its device memory (and the compile's
+ * scratch) comes from a stream-ordered memory pool the library keeps per
+ * device, so no step of the compile synchronises the whole device.  *out
+ * receives a new handle on success and is untouched on failure. */
 BSA_API bsa_status bsa_mask_compile(const bsa_mask_spec* spec, const bsa_mask_opts* opts, bsa_stream stream,
                             bsa_mask_info** out);
 BSA_API bsa_status bsa_mask_info_view(const bsa_mask_info* info, bsa_mask_info_desc* out);
-/* Frees the handle's device storage (synchronises the device). NULL is accepted. */
+/* Returns the handle's device storage to the library's pool (synchronises
+ * the device first, so no launch still reads it). NULL is accepted. */
 BSA_API bsa_status bsa_mask_info_destroy(bsa_mask_info* info);
 
 typedef struct {
@@ -168,8 +171,9 @@ typedef struct {
  * previous kernel on `stream`, and it waits for that kernel before reading
  * Q/K/V or writing O/LSE (BSA_PDL=0 in the environment turns this off).
  * The first launch of a (B, Hq, SM count) configuration builds its tile
- * schedule (a small synchronous allocation and upload, cached in the
- * MaskInfo). */
+ * schedule on the host and uploads it in stream order on `stream` (cached
+ * in the MaskInfo; a later launch on another stream waits for the upload
+ * through an event). */
 BSA_API bsa_status bsa_fwd(const bsa_fwd_args* args, const bsa_mask_info* fwd_info, bsa_stream stream);
 
 /* One shard of the key axis ("Splash Attention: When the Mask Stops Being
@@ -266,8 +270,8 @@ BSA_API bsa_status bsa_bwd_rowsum(const bsa_bwd_args* args, bsa_stream stream);
  * the library keeps per device (cudaMallocFromPoolAsync, returned with
  * cudaFreeAsync on `stream`, kept cached by the pool) and a second kernel
  * adds them up in a fixed order.  The first launch of a configuration also
- * builds its tile schedule (a small synchronous allocation and upload,
- * cached in the MaskInfo); bsa_bwd_noalloc does neither. */
+ * builds its tile schedule (uploaded in stream order, cached in the
+ * MaskInfo, as for bsa_fwd); bsa_bwd_noalloc does neither. */
 BSA_API bsa_status bsa_bwd_dkv(const bsa_bwd_args* args, const bsa_mask_info* dkv_info, bsa_stream stream);
 /* dQ: grid over (b, query head, query block), keys innermost.  The first
  * launch of a configuration builds its tile schedule (cached in the MaskInfo,
