@@ -191,6 +191,26 @@ def run_gpu(args):
         i2.destroy()
         d2.destroy()
     compile_ms = sorted(warm)[len(warm) // 2]
+    # The dense-mask compiler on a large mask, where reading it dominates:
+    # 16384 x 16384 bytes (256 MiB) of a causal pattern (all 128 diagonal
+    # blocks partial and equal), forward orientation, warm median of 3.
+    big_s = 16384
+    idx = torch.arange(big_s, device=dev)
+    big = (idx[:, None] >= idx[None, :]).to(torch.uint8)
+    del idx
+    bsa.mask_compile("dense", big_s, big_s, dense=big).destroy()
+    dense_ms = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        bsa.mask_compile("dense", big_s, big_s, dense=big).destroy()
+        dense_ms.append((time.perf_counter() - t0) * 1e3)
+    del big
+    dense_compile_ms = sorted(dense_ms)[1]
+    dense_compile = {"S": big_s, "mask_bytes": big_s * big_s, "ms": round(dense_compile_ms, 3),
+                     "gbs": round(big_s * big_s / (dense_compile_ms * 1e-3) / 1e9, 1),
+                     "note": "whole compile (classify, dedup, next-block and shrink passes, host syncs) of a "
+                             "causal-pattern byte mask; GB/s = mask bytes / compile time"}
     d = info.desc()
     n_exec = (d.n_partial + d.n_full) // d.heads
     f_fwd, f_bwd = flops(w, n_exec)
@@ -312,6 +332,7 @@ def run_gpu(args):
             "rowsum_gbs": round(rowsum_bytes / (ms["rowsum"] * 1e-3) / 1e9, 1),
             "mask_compile_ms": round(compile_ms, 3),
             "mask_compile_note": "both orientations, warm median of 3 (first, cold: %.3f ms)" % compile_cold_ms,
+            "mask_dense_compile": dense_compile,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
