@@ -20,18 +20,22 @@
 //       S = Q K^T, dP = dO V^T, dQ += dS K
 // dK and dQ take the softmax scale at the end.
 //
-// GB300 design (one persistent CTA per SM, 12 warps):
+// GB300 design (one persistent CTA per SM, warp-specialised):
 //   warp 0      TMA producer; also the only reader of MaskInfo: it publishes
 //               each block's descriptor into a shared-memory ring
 //   warp 1      tcgen05 issuer, warp-converged, one elected lane issues
 //   warp 2      second TMA producer (V blocks of the dQ launch)
-//   warps 4-11  two warpgroups, one (tile row, half of the 128 columns) per
+//   warps 4-    kParts elementwise warpgroups (4 for D = 128, 2 for D = 64),
+//               one (tile row, 128 / kParts of the score columns) per
 //               thread: rebuild P and dS from the scores in TMEM and write
 //               them back to TMEM as bf16, where they are the A operand of
-//               the accumulating MMAs; each half writes inside its own
-//               64-column range (words at columns [64h, 64h+32)), so the two
-//               halves never race and the MMA reads the A operand in two
-//               32-column pieces.
+//               the accumulating MMAs; each part writes inside its own
+//               column range, so the parts never race, and the MMA reads the
+//               A operand in per-part pieces.  The dK/dV launch publishes
+//               P^T in two halves per thread, so that dV starts on the first
+//               half.  At a tile's end the same warps run the epilogue: bf16
+//               dK/dV through shared memory and tensor stores, dQ with
+//               32-byte stores.
 // All MMAs are 128 x 128 (full rate on sm_103a).
 #include <cmath>
 
