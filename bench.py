@@ -158,6 +158,127 @@ class Clocks:
                 "samples": len(sm)}
 
 
+class Prepared:
+    """One workload's inputs, compiled MaskInfo (both orientations) and output
+    buffers, resident on the device."""
+
+    def __init__(self, bsa, w, dev, seed_offset=0):
+        self.bsa, self.w, self.dev = bsa, w, dev
+        self.q, self.k, self.v, self.do = qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed + seed_offset)
+        self.dense_h = bernoulli_mask(w.S, w.mask.p, w.mask.seed) if w.mask.kind == "dense" else None
+        self.qd, self.kd, self.vd, self.dod = (t.to(dev) for t in (self.q, self.k, self.v, self.do))
+        self.dense_d = None if self.dense_h is None else torch.from_numpy(self.dense_h).to(dev)
+        t0 = time.perf_counter()
+        self.info, self.dkv = self.compile()
+        torch.cuda.synchronize()
+        self.compile_cold_ms = (time.perf_counter() - t0) * 1e3
+        warm = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            i2, d2 = self.compile()
+            torch.cuda.synchronize()
+            warm.append((time.perf_counter() - t0) * 1e3)
+            i2.destroy()
+            d2.destroy()
+        self.compile_ms = sorted(warm)[1]
+        d = self.info.desc()
+        self.n_exec = (d.n_partial + d.n_full) // d.heads
+        self.o = torch.empty_like(self.qd)
+        self.lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+        self.dq = torch.empty_like(self.qd)
+        self.dk = torch.empty_like(self.kd)
+        self.dv = torch.empty_like(self.vd)
+        self.dsum = torch.empty_like(self.lse)
+
+    def compile(self):
+        w, bsa = self.w, self.bsa
+        info = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=self.dense_d, **mask_kwargs(w))
+        dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=self.dense_d, orientation="dkv", **mask_kwargs(w))
+        return info, dkv
+
+    def step(self, stream, evs=None):
+        """forward, rowsum, dK/dV, dQ; with `evs` (5 events) one between launches."""
+        bsa = self.bsa
+        if evs is not None:
+            evs[0].record(stream)
+        bsa.fwd(self.qd, self.kd, self.vd, self.info, o=self.o, lse=self.lse)
+        if evs is not None:
+            evs[1].record(stream)
+        bsa.bwd_rowsum(self.o, self.dod, dsum=self.dsum)
+        if evs is not None:
+            evs[2].record(stream)
+        bsa.bwd_dkv(self.qd, self.kd, self.vd, self.o, self.lse, self.dod, self.dsum, self.dkv, dk=self.dk,
+                    dv=self.dv)
+        if evs is not None:
+            evs[3].record(stream)
+        bsa.bwd_dq(self.qd, self.kd, self.vd, self.o, self.lse, self.dod, self.dsum, self.info, dq=self.dq)
+        if evs is not None:
+            evs[4].record(stream)
+
+    def time_steps(self, stream, flush, n):
+        """Whole steps, events only at step boundaries; L2 flushed between
+        steps outside the events.  Returns the per-step times in ms."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            evs[i][0].record(stream)
+            self.step(stream)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in evs]
+
+    def time_kernels(self, stream, flush, n):
+        """The same steps with an event between launches: mean ms per kernel."""
+        kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            self.step(stream, kevs[i])
+        torch.cuda.synchronize()
+        per = {"fwd": [], "rowsum": [], "dkv": [], "dq": [], "step": []}
+        for e in kevs:
+            per["fwd"].append(e[0].elapsed_time(e[1]))
+            per["rowsum"].append(e[1].elapsed_time(e[2]))
+            per["dkv"].append(e[2].elapsed_time(e[3]))
+            per["dq"].append(e[3].elapsed_time(e[4]))
+            per["step"].append(e[0].elapsed_time(e[4]))
+        return {k: sum(v) / len(v) for k, v in per.items()}
+
+
+# Backward work split between the two launches in proportion to the GEMMs each
+# executes (dK/dV: S^T, dP^T, dV, dK; dQ: S, dP, dQ): the algorithmic
+# backward is 5 GEMMs of the 7 executed, so each launch is credited 5/7 of
+# its executed FLOP.
+ALG_BWD = 5.0 / 7.0
+
+
+def kernel_table(w, n_exec, ms, pk, mhz, n_sms):
+    """Per-kernel throughput for one workload: algorithmic TFLOP/s and its
+    fraction of the measured bf16 peak, executed ("hardware") TFLOP/s, and SM
+    cycles per executed block and q head at the sampled SM clock."""
+    gemm = n_exec * w.B * w.Hq * 2 * 128 * 128 * w.D
+    executed = {"fwd": 2 * gemm, "dkv": 4 * gemm, "dq": 3 * gemm}
+    alg = {"fwd": 2 * gemm, "dkv": 4 * gemm * ALG_BWD, "dq": 3 * gemm * ALG_BWD}
+    blocks = n_exec * w.B * w.Hq
+    out = {}
+    for k in executed:
+        t = ms[k] * 1e-3
+        out[k] = {"ms": round(ms[k], 4),
+                  "tflops_alg": round(alg[k] / t / 1e12, 1),
+                  "frac_alg": round(alg[k] / t / 1e12 / pk["bf16_tflops"], 4),
+                  "tflops_executed": round(executed[k] / t / 1e12, 1),
+                  "frac_executed": round(executed[k] / t / 1e12 / pk["bf16_tflops"], 4)}
+        if mhz:
+            out[k]["sm_cycles_per_block"] = round(t * mhz * 1e6 * n_sms / blocks, 1)
+            out[k]["tensor_cycles_per_block"] = {"fwd": 2, "dkv": 4, "dq": 3}[k] * 2 * 128 * 128 * w.D // 8192
+    bwd_ms = ms["rowsum"] + ms["dkv"] + ms["dq"]
+    out["bwd"] = {"ms": round(bwd_ms, 4), "tflops_alg": round(5 * gemm / (bwd_ms * 1e-3) / 1e12, 1),
+                  "frac_alg": round(5 * gemm / (bwd_ms * 1e-3) / 1e12 / pk["bf16_tflops"], 4)}
+    out["rowsum"] = {"ms": round(ms["rowsum"], 4),
+                     "gbs": round((4 * w.B * w.Hq * w.S * w.D + 4 * w.B * w.Hq * w.S) / (ms["rowsum"] * 1e-3) / 1e9,
+                                  1)}
+    return out
+
+
 def run_gpu(args):
     import block_sparse_attention_process_gb300 as bsa
     ws, rank, local = dist_env()
@@ -168,144 +289,86 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
     pk = peaks()
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     # ---------------------------------------------------------------- inputs (resident in HBM)
-    q, k, v, do = qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed + rank)
-    dense_h = bernoulli_mask(w.S, w.mask.p, w.mask.seed) if w.mask.kind == "dense" else None
-    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
-    dense_d = None if dense_h is None else torch.from_numpy(dense_h).to(dev)
-
-    t0 = time.perf_counter()
-    info = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dense_d, **mask_kwargs(w))
-    dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dense_d, orientation="dkv", **mask_kwargs(w))
-    torch.cuda.synchronize()
-    compile_cold_ms = (time.perf_counter() - t0) * 1e3
-    # warm: both orientations again (what a compile costs once the library is loaded)
-    warm = []
-    for _ in range(3):
-        t0 = time.perf_counter()
-        i2 = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dense_d, **mask_kwargs(w))
-        d2 = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dense_d, orientation="dkv", **mask_kwargs(w))
-        torch.cuda.synchronize()
-        warm.append((time.perf_counter() - t0) * 1e3)
-        i2.destroy()
-        d2.destroy()
-    compile_ms = sorted(warm)[len(warm) // 2]
-    # The dense-mask compiler on a large mask, where reading it dominates:
-    # 16384 x 16384 bytes (256 MiB) of a causal pattern (all 128 diagonal
-    # blocks partial and equal), forward orientation, warm median of 3.
-    big_s = 16384
-    idx = torch.arange(big_s, device=dev)
-    big = (idx[:, None] >= idx[None, :]).to(torch.uint8)
-    del idx
-    bsa.mask_compile("dense", big_s, big_s, dense=big).destroy()
-    dense_ms = []
-    for _ in range(3):
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        bsa.mask_compile("dense", big_s, big_s, dense=big).destroy()
-        dense_ms.append((time.perf_counter() - t0) * 1e3)
-    del big
-    dense_compile_ms = sorted(dense_ms)[1]
-    dense_compile = {"S": big_s, "mask_bytes": big_s * big_s, "ms": round(dense_compile_ms, 3),
-                     "gbs": round(big_s * big_s / (dense_compile_ms * 1e-3) / 1e9, 1),
-                     "note": "whole compile (classify, dedup, next-block and shrink passes, host syncs) of a "
-                             "causal-pattern byte mask; GB/s = mask bytes / compile time"}
-    d = info.desc()
-    n_exec = (d.n_partial + d.n_full) // d.heads
+    P = Prepared(bsa, w, dev, seed_offset=rank)
+    dense_compile = big_dense_compile(bsa, dev)
+    n_exec = P.n_exec
     f_fwd, f_bwd = flops(w, n_exec)
-
-    o = torch.empty_like(qd)
-    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
-    dq = torch.empty_like(qd)
-    dk = torch.empty_like(kd)
-    dv = torch.empty_like(vd)
-    dsum = torch.empty_like(lse)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    n_ev = 5
-    def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
-        bsa.fwd(qd, kd, vd, info, o=o, lse=lse)
-        if evs is not None:
-            evs[1].record(stream)
-        bsa.bwd_rowsum(o, dod, dsum=dsum)
-        if evs is not None:
-            evs[2].record(stream)
-        bsa.bwd_dkv(qd, kd, vd, o, lse, dod, dsum, dkv, dk=dk, dv=dv)
-        if evs is not None:
-            evs[3].record(stream)
-        bsa.bwd_dq(qd, kd, vd, o, lse, dod, dsum, info, dq=dq)
-        if evs is not None:
-            evs[4].record(stream)
-
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        P.step(stream)
     assert bsa.get_device_error() == 0
 
     # ---------------------------------------------------------------- timed region
     # Whole steps, events only at the step boundaries (the four launches of
     # a step follow each other as they would in training).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
-        for i in range(args.steps):
-            flush.zero_()          # L2 flush between steps (outside the events)
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
+        step_times = P.time_steps(stream, flush, args.steps)
     if ws > 1:
         torch.distributed.barrier()
     assert bsa.get_device_error() == 0
-    step_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
+    step_ms = sum(step_times) / len(step_times)
+    clocks = clk.summary()
 
     # Per-kernel breakdown (roofline of the dominant kernel): the same steps
     # again with an event between launches.
-    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        step(kevs[i])
-    torch.cuda.synchronize()
+    with Clocks(local) as kclk:
+        ms = P.time_kernels(stream, flush, args.steps)
     assert bsa.get_device_error() == 0
-    per = {"fwd": [], "rowsum": [], "dkv": [], "dq": [], "step": []}
-    for e in kevs:
-        per["fwd"].append(e[0].elapsed_time(e[1]))
-        per["rowsum"].append(e[1].elapsed_time(e[2]))
-        per["dkv"].append(e[2].elapsed_time(e[3]))
-        per["dq"].append(e[3].elapsed_time(e[4]))
-        per["step"].append(e[0].elapsed_time(e[4]))
-    ms = {k: sum(v) / len(v) for k, v in per.items()}
+    kclocks = kclk.summary()
     step_ms = max_over_ranks(step_ms, dev)
     value = job_tflops(f_fwd + f_bwd, step_ms * 1e-3, ws)
+    mhz = kclocks["sm_mhz"] or clocks["sm_mhz"]
+    table = kernel_table(w, n_exec, ms, pk, mhz, n_sms)
 
-    # per-kernel algorithmic work: executed GEMMs of 2*128*128*D FLOP per block and q head
-    gemm = n_exec * w.B * w.Hq * 2 * 128 * 128 * w.D
-    kern = {
-        "fwd": {"flop": 2 * gemm, "ms": ms["fwd"]},
-        "dkv": {"flop": 4 * gemm, "ms": ms["dkv"]},
-        "dq": {"flop": 3 * gemm, "ms": ms["dq"]},
-    }
-    rowsum_bytes = 4 * w.B * w.Hq * w.S * w.D + 4 * w.B * w.Hq * w.S
-    dom = max(kern, key=lambda k: kern[k]["ms"])
-    achieved = kern[dom]["flop"] / (kern[dom]["ms"] * 1e-3) / 1e12
+    dom = max(("fwd", "dkv", "dq"), key=lambda k: ms[k])
     traffic = traffic_per_launch(args.workload, dom)
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
-                "peak_source": f"{pk['source']} bf16 burst"}
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": table[dom]["tflops_alg"], "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": table[dom]["frac_alg"], "traffic": traffic,
+                "frac_algorithmic": table[dom]["frac_alg"],
+                "achieved_executed": table[dom]["tflops_executed"], "frac_executed": table[dom]["frac_executed"],
+                "count": "algorithmic: forward 2 GEMMs per executed block and q head; backward 5 GEMMs, each "
+                         "launch credited 5/7 of the GEMMs it executes (dK/dV 4, dQ 3); executed = every GEMM run",
+                "sm_cycles_per_block": table[dom].get("sm_cycles_per_block"),
+                "peak_source": f"{pk['source']} bf16 burst (of measured)" if pk["source"] == "measured"
+                else "fallback bf16 burst"}
+
+    # ---------------------------------------------------------------- sustained: seconds of steps
+    sustained = None
+    if args.sustained_s > 0:
+        n = max(args.steps, int(math.ceil(args.sustained_s * 1e3 / max(step_ms, 1e-3))))
+        torch.cuda.synchronize()
+        with Clocks(local) as sclk:
+            st = P.time_steps(stream, flush, n)
+        assert bsa.get_device_error() == 0
+        s_ms = sum(st) / len(st)
+        s_val = (f_fwd + f_bwd) / (s_ms * 1e-3) / 1e12
+        peak_s = pk["bf16_sustained"] or pk["bf16_tflops"]
+        sustained = {"steps": n, "seconds": round(sum(st) * 1e-3, 2), "ms_per_step": round(s_ms, 4),
+                     "value": round(s_val, 2), "unit": "TFLOP/s", "peak": peak_s,
+                     "frac": round(s_val / peak_s, 4), "peak_source": "measured bf16 sustained",
+                     "clocks": sclk.summary()}
+
+    # ---------------------------------------------------------------- the other workloads
+    others = {}
+    if not args.no_workloads and ws == 1:
+        others = other_workloads(bsa, args, dev, pk, n_sms, flush, stream)
 
     # ---------------------------------------------------------------- end to end through the public API
-    e2e = run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, f_fwd + f_bwd, ws)
+    e2e = run_e2e(bsa, w, P.q, P.k, P.v, P.do, P.dense_h, dev, args, f_fwd + f_bwd, ws)
 
     out = None
     if rank == 0:
-        cpu = None if args.no_cpu_baseline or ws > 1 else cpu_baseline(w, dense_h, n_exec, seconds=args.cpu_seconds)
+        cpu = None if args.no_cpu_baseline or ws > 1 else cpu_baseline(w, P.dense_h, n_exec,
+                                                                       seconds=args.cpu_seconds)
         out = {
             "metric": METRIC,
             "value": round(value, 2),
@@ -326,22 +389,84 @@ def run_gpu(args):
             "frac_of_peak": round(value / pk["bf16_tflops"], 4),
             "kernels_ms": {k: round(v, 4) for k, v in ms.items()},
             "kernels_note": "kernels_ms from a second pass with an event between launches; value from whole steps",
-            "kernels_tflops": {k: round(kern[k]["flop"] / (kern[k]["ms"] * 1e-3) / 1e12, 1) for k in kern},
-            "fwd_tflops": round(f_fwd / (ms["fwd"] * 1e-3) / 1e12, 1),
-            "bwd_tflops": round(f_bwd / ((ms["rowsum"] + ms["dkv"] + ms["dq"]) * 1e-3) / 1e12, 1),
-            "rowsum_gbs": round(rowsum_bytes / (ms["rowsum"] * 1e-3) / 1e9, 1),
-            "mask_compile_ms": round(compile_ms, 3),
-            "mask_compile_note": "both orientations, warm median of 3 (first, cold: %.3f ms)" % compile_cold_ms,
+            "kernels": table,
+            "fwd_tflops": table["fwd"]["tflops_alg"],
+            "bwd_tflops": table["bwd"]["tflops_alg"],
+            "rowsum_gbs": table["rowsum"]["gbs"],
+            "mask_compile_ms": round(P.compile_ms, 3),
+            "mask_compile_note": "both orientations, warm median of 3 (first, cold: %.3f ms)" % P.compile_cold_ms,
             "mask_dense_compile": dense_compile,
             "roofline": roofline,
+            "sustained": sustained,
+            "workloads": others,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 4 * args.steps,
-            "clocks": clk.summary(),
+            "clocks": clocks,
+            "clocks_kernel_pass": kclocks,
         }
         print(json.dumps(out), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+    return out
+
+
+def big_dense_compile(bsa, dev):
+    """The dense-mask compiler on a large mask, where reading it dominates:
+    16384 x 16384 bytes (256 MiB) of a causal pattern (all 128 diagonal
+    blocks partial and equal), forward orientation, warm median of 3."""
+    big_s = 16384
+    idx = torch.arange(big_s, device=dev)
+    big = (idx[:, None] >= idx[None, :]).to(torch.uint8)
+    del idx
+    bsa.mask_compile("dense", big_s, big_s, dense=big).destroy()
+    dense_ms = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        bsa.mask_compile("dense", big_s, big_s, dense=big).destroy()
+        dense_ms.append((time.perf_counter() - t0) * 1e3)
+    del big
+    ms = sorted(dense_ms)[1]
+    return {"S": big_s, "mask_bytes": big_s * big_s, "ms": round(ms, 3),
+            "gbs": round(big_s * big_s / (ms * 1e-3) / 1e9, 1),
+            "note": "whole compile (classify, dedup, next-block and shrink passes, host syncs) of a "
+                    "causal-pattern byte mask; GB/s = mask bytes / compile time"}
+
+
+def other_workloads(bsa, args, dev, pk, n_sms, flush, stream):
+    """Every workload but the headline one, measured in the same run: forward,
+    dK/dV, dQ and backward throughput at the algorithmic count, per-kernel
+    times, SM cycles per block, mask compile time and the oracle timed on
+    the host cores on a bounded sample of that workload."""
+    out = {}
+    for name in sorted(WORKLOADS):
+        if name == args.workload:
+            continue
+        w = WORKLOADS[name]
+        P = Prepared(bsa, w, dev)
+        for _ in range(args.warmup):
+            flush.zero_()
+            P.step(stream)
+        with Clocks(dev.index) as clk:
+            ms = P.time_kernels(stream, flush, max(args.steps, 10))
+            st = P.time_steps(stream, flush, max(args.steps, 10))
+        assert bsa.get_device_error() == 0
+        c = clk.summary()
+        f_fwd, f_bwd = flops(w, P.n_exec)
+        step_ms = sum(st) / len(st)
+        ent = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "mask": w.mask.kind,
+               "executed_blocks_per_head": P.n_exec,
+               "step_ms": round(step_ms, 4), "step_tflops": round((f_fwd + f_bwd) / (step_ms * 1e-3) / 1e12, 1),
+               "kernels": kernel_table(w, P.n_exec, ms, pk, c["sm_mhz"], n_sms),
+               "mask_compile_ms": round(P.compile_ms, 3), "clocks": c}
+        if w.mask.kind == "dense":
+            ent["mask_compile_gbs"] = round(2 * w.S * w.S / (P.compile_ms * 1e-3) / 1e9, 1)
+        if not args.no_cpu_baseline:
+            ent["cpu_baseline"] = cpu_baseline(w, P.dense_h, P.n_exec, seconds=args.cpu_seconds_other)
+        out[name] = ent
+        del P
+        torch.cuda.empty_cache()
     return out
 
 
@@ -553,7 +678,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds-other", type=float, default=5.0,
+                    help="oracle seconds per workload in the 'workloads' table")
+    ap.add_argument("--sustained-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps timed against the sustained bf16 peak (0: off)")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ingest-ncu", metavar="REPORT",
                     help="write profiles/traffic.json for --workload from an ncu report of this bench, then exit")

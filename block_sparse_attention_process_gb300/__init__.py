@@ -260,20 +260,22 @@ def bwd(q, k, v, o, lse, do, fwd_info: MaskInfo, dkv_info: MaskInfo, *, dq=None,
 
 
 def bwd_noalloc(q, k, v, o, lse, do, fwd_info: MaskInfo, dkv_info: MaskInfo, *, dq, dk, dv, softmax_scale=None,
-                grad_fp32: bool = False, stream=None):
+                grad_fp32: bool = False, logits_soft_cap=None, sinks=None, dsinks=None, stream=None):
     """bsa_bwd_noalloc: the backward pass with no device allocation inside the
     library (its rowsum scratch is a fixed 4 MiB device array); the caller
-    supplies the gradient buffers."""
+    supplies the gradient buffers (and ``dsinks``, the sinks' shape, when the
+    sinks' gradient is wanted)."""
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check_bf16(n, t)
     B, Hq, S, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
+    sp, sn, skv = _sink_fields(sinks, Hkv)
     a = _abi.BwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
                      None, B, Hq, Hkv, D, S, Skv, math.nan if softmax_scale is None else softmax_scale,
-                     1 if grad_fp32 else 0)
+                     1 if grad_fp32 else 0, logits_soft_cap or 0.0, sp, _ptr(dsinks), sn, skv)
     check(_abi.lib().bsa_bwd_noalloc(C.byref(a), fwd_info.handle, dkv_info.handle, _stream(stream)),
           "bsa_bwd_noalloc")
-    return dq, dk, dv
+    return (dq, dk, dv) if dsinks is None else (dq, dk, dv, dsinks)
 
 
 def bwd_rowsum(o, do, *, dsum=None, stream=None) -> torch.Tensor:

@@ -3,7 +3,9 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <set>
 #include <string>
+#include <utility>
 
 #include <cstdlib>
 
@@ -27,6 +29,15 @@ bsa_status fail(bsa_status s, const std::string& msg) {
 bsa_status cuda_fail(cudaError_t e, const char* what) {
   set_last_error(std::string(what) + ": " + cudaGetErrorString(e));
   return e == cudaErrorMemoryAllocation ? BSA_ERR_OOM : BSA_ERR_CUDA;
+}
+
+// The library's error word of the current device if a launch there has
+// already allocated it (a reader need not allocate: no word, no error).
+uint32_t* device_error_word_if_set() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  return g_err_word[dev];
 }
 
 uint32_t* device_error_word() {
@@ -87,6 +98,20 @@ bool pdl_enabled() {
     return !(e && e[0] == '0');
   }();
   return on;
+}
+
+bsa_status ensure_smem_attr(const void* func, size_t smem, const char* what) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({dev, func})) return BSA_OK;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  done.insert({dev, func});
+  return BSA_OK;
 }
 
 int num_sms() {
@@ -168,11 +193,13 @@ bsa_status check_transforms(float cap, const float* sinks, int32_t num_sinks) {
   return BSA_OK;
 }
 
-bsa_status check_bwd(const bsa_bwd_args* a) {
+}  // namespace
+
+bsa_status bsa::check_bwd_args(const bsa_bwd_args* a, bool need_dsum) {
   if (!a) return fail(BSA_ERR_INVALID_ARG, "args is null");
   bsa_status s = check_shapes(a->B, a->Hq, a->Hkv, a->S_q, a->S_kv, a->D);
   if (s != BSA_OK) return s;
-  const void* ptrs[] = {a->q, a->k, a->v, a->o, a->lse, a->do_, a->dq, a->dk, a->dv, a->dsum};
+  const void* ptrs[] = {a->q, a->k, a->v, a->o, a->lse, a->do_, a->dq, a->dk, a->dv, need_dsum ? a->dsum : a->q};
   for (const void* p : ptrs)
     if (!p) return fail(BSA_ERR_INVALID_ARG, "a tensor pointer is null");
   for (const void* p : ptrs)
@@ -184,6 +211,8 @@ bsa_status check_bwd(const bsa_bwd_args* a) {
   return BSA_OK;
 }
 
+namespace {
+bsa_status check_bwd(const bsa_bwd_args* a) { return check_bwd_args(a, true); }
 }  // namespace
 
 extern "C" {
@@ -216,16 +245,22 @@ bsa_status bsa_debug_wait_timeout(bsa_stream stream) {
 
 bsa_status bsa_get_device_error(bsa_stream stream, uint32_t* word) {
   if (!word) return fail(BSA_ERR_INVALID_ARG, "word is null");
-  uint32_t* d = device_error_word();
-  if (!d) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  // both words of the current device: the one of the ordinary launches and
+  // the one of the allocation-free backward; neither is allocated here
   uint32_t h = 0;
-  e = cudaMemcpy(&h, d, sizeof(h), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
-  e = cudaMemset(d, 0, sizeof(uint32_t));
-  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  uint32_t* words[2] = {device_error_word_if_set(), noalloc_error_word_if_set()};
+  for (uint32_t* d : words) {
+    if (!d) continue;
+    uint32_t x = 0;
+    e = cudaMemcpy(&x, d, sizeof(x), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    e = cudaMemset(d, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    h |= x;
+  }
   *word = h;
   if (h & DEV_ERR_TIMEOUT) return fail(BSA_ERR_TIMEOUT, "a device-side wait ran out");
   if (h) return fail(BSA_ERR_DEVICE, "a kernel reported a device-side error");

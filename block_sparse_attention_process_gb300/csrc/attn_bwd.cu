@@ -1398,11 +1398,9 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
   auto kern = variant == 2 ? dkv_kernel<D, true, kAnyMask>
                            : (variant == 1 ? dkv_kernel<D, false, kDenseMask> : dkv_kernel<D, false, kComputableMask>);
   const size_t smem = sizeof(DkvSmem<D>) + 1024;
-  static bool attr_set[3] = {false, false, false};
-  if (!attr_set[variant]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "set dkv smem size");
-    attr_set[variant] = true;
+  {
+    bsa_status st = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, "set dkv smem size");
+    if (st != BSA_OK) return st;
   }
   // With few KV tiles (MQA, short sequences) the q heads of a group are
   // split over several CTAs: the smallest divisor of the group that gives
@@ -1474,11 +1472,9 @@ bsa_status launch_dq(const bsa_bwd_args* a, const bsa_mask_info* info, float sca
   auto kern = variant == 2 ? dq_kernel<D, true, kAnyMask>
                            : (variant == 1 ? dq_kernel<D, false, kDenseMask> : dq_kernel<D, false, kComputableMask>);
   const size_t smem = sizeof(DqSmem<D>) + 1024;
-  static bool attr_set[3] = {false, false, false};
-  if (!attr_set[variant]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "set dq smem size");
-    attr_set[variant] = true;
+  {
+    bsa_status st = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, "set dq smem size");
+    if (st != BSA_OK) return st;
   }
   const int grid = std::min(p.n_tiles, num_sms());
   if (schedule) {

@@ -844,11 +844,9 @@ bsa_status launch_fwd(const FwdCall& c, const bsa_mask_info* info, float scale, 
   auto kern = variant == 2 ? fwd_kernel<D, true, false>
                            : (variant == 1 ? fwd_kernel<D, false, true> : fwd_kernel<D, false, false>);
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  static bool attr_set[3] = {false, false, false};
-  if (!attr_set[variant]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "set forward smem size");
-    attr_set[variant] = true;
+  {
+    bsa_status st = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, "set forward smem size");
+    if (st != BSA_OK) return st;
   }
   const int grid = std::min(p.n_tiles, num_sms());
   bsa_status st = tile_schedule(info, c.B, c.Hq, 1, 1, grid, stream, &p.sched, &p.sched_stride);

@@ -73,6 +73,20 @@ bsa_status debug_wait_timeout_launch(cudaStream_t stream);
 
 int num_sms();
 
+// Raises `func`'s dynamic shared-memory limit to `smem` bytes on the current
+// device, once per (device, kernel): the attribute is per device, so a
+// process that launches on several GPUs sets it on each.
+bsa_status ensure_smem_attr(const void* func, size_t smem, const char* what);
+
+// Host-side checks of a backward call's arguments (shapes, pointers and
+// their alignment, score transforms); `need_dsum` false for the entry point
+// that keeps the rowsum in its own scratch.
+bsa_status check_bwd_args(const bsa_bwd_args* a, bool need_dsum);
+
+// The allocation-free backward's device error word on the current device,
+// or null when no call there has set it up yet.
+uint32_t* noalloc_error_word_if_set();
+
 // Work tiles of a launch: (b, g, MaskInfo row i, split) for b < n_b, g < n_g
 // and split < splits, each covering group / splits mask heads (the q heads
 // of a KV group in the dK/dV launch, split over `splits` CTAs when the

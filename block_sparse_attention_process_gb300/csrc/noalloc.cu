@@ -3,7 +3,7 @@
 // The ordinary backward needs two pieces of device memory besides its
 // inputs and outputs: the rowsum(dO*O) workspace (which the caller passes)
 // and the library's device error word (which the library allocates on the
-// first call on each device).  Here both live in file-scope device arrays
+// first launch on each device).  Here both live in file-scope device arrays
 // that exist from the moment the library is loaded on a device until the
 // process exits, so a call allocates and frees nothing.  The host only
 // needs their device addresses, which cudaGetSymbolAddress gives; that
@@ -22,7 +22,8 @@ constexpr int64_t kMaxRows = int64_t(1) << 20;
 
 // Shared by every call on a device; holds the last call's rowsum.
 static __device__ __align__(256) float g_dsum_scratch[kMaxRows];
-// Device-side error bits of this entry point's kernels (cleared by each call).
+// Device-side error bits of this entry point's kernels; they stay set until
+// bsa_get_device_error reads and clears them (with the library's own word).
 static __device__ __align__(256) uint32_t g_err_scratch;
 
 std::mutex g_mu;
@@ -53,30 +54,14 @@ bsa_status resolve(float** dsum, uint32_t** err) {
   return BSA_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 bsa_status check(const bsa_bwd_args* a, const bsa_mask_info* fwd_info, const bsa_mask_info* dkv_info) {
-  if (!a) return fail(BSA_ERR_INVALID_ARG, "args is null");
-  if (a->B <= 0 || a->Hq <= 0 || a->Hkv <= 0) return fail(BSA_ERR_INVALID_ARG, "B, Hq and Hkv must be positive");
-  if (a->Hq % a->Hkv != 0) return fail(BSA_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
-  if (a->S_q <= 0 || a->S_kv <= 0 || a->S_q % kBlock || a->S_kv % kBlock)
-    return fail(BSA_ERR_INVALID_ARG, "sequence lengths must be positive multiples of 128");
-  if (a->D != 64 && a->D != 128) return fail(BSA_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+  // the same checks as the ordinary backward, without the dsum workspace
+  bsa_status s = check_bwd_args(a, false);
+  if (s != BSA_OK) return s;
   const int64_t rows = static_cast<int64_t>(a->B) * a->Hq * a->S_q;
   if (rows > kMaxRows)
     return fail(BSA_ERR_UNSUPPORTED, "bsa_bwd_noalloc: B*Hq*S_q = " + std::to_string(rows) +
                                          " exceeds its fixed scratch of 1048576 rows; use bsa_bwd");
-  if (static_cast<int64_t>(a->B) * a->Hkv * a->S_kv > static_cast<int64_t>(INT32_MAX))
-    return fail(BSA_ERR_UNSUPPORTED, "B*Hkv*S_kv must fit in int32");
-  const void* ptrs[] = {a->q, a->k, a->v, a->o, a->lse, a->do_, a->dq, a->dk, a->dv};
-  for (const void* p : ptrs)
-    if (!p) return fail(BSA_ERR_INVALID_ARG, "a tensor pointer is null");
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return fail(BSA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  if (!(a->logits_soft_cap >= 0.f) || std::isinf(a->logits_soft_cap))
-    return fail(BSA_ERR_INVALID_ARG, "logits_soft_cap must be finite and >= 0");
-  if (a->num_sinks < 0 || a->num_sinks > 64) return fail(BSA_ERR_UNSUPPORTED, "num_sinks must be in 0..64");
-  if (a->num_sinks > 0 && !a->sinks) return fail(BSA_ERR_INVALID_ARG, "sinks is null");
   const bsa_mask_info* infos[2] = {fwd_info, dkv_info};
   const int32_t orient[2] = {BSA_ORIENT_FWD, BSA_ORIENT_DKV};
   for (int i = 0; i < 2; ++i) {
@@ -91,6 +76,14 @@ bsa_status check(const bsa_bwd_args* a, const bsa_mask_info* fwd_info, const bsa
 }
 
 }  // namespace
+
+uint32_t* noalloc_error_word_if_set() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_err_ptr[dev];
+}
+
 }  // namespace bsa
 
 using namespace bsa;
@@ -104,8 +97,6 @@ extern "C" bsa_status bsa_bwd_noalloc(const bsa_bwd_args* a, const bsa_mask_info
   s = resolve(&dsum, &err);
   if (s != BSA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), st);
-  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
   bsa_bwd_args b;
   std::memcpy(&b, a, sizeof(b));
   b.dsum = dsum;  // every row is rewritten by the rowsum kernel before it is read

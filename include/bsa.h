@@ -295,16 +295,22 @@ BSA_API bsa_status bsa_bwd_dq(const bsa_bwd_args* args, const bsa_mask_info* fwd
  *     it): calls that overlap on the GPU race, so serialise them (one
  *     stream, or events).
  *   - Device-side error bits of this entry point (a wait that ran out, a bad
- *     MaskInfo index) go to a device word of its own, also static and
- *     cleared at the start of each call; bsa_get_device_error does not
- *     report them.  Host-side argument errors are returned as for bsa_bwd. */
+ *     MaskInfo index) go to a device word of its own, also static; they
+ *     stay set until bsa_get_device_error reads and clears them (it reads
+ *     this word together with the library's own and allocates neither).
+ *     Host-side argument errors are returned as for bsa_bwd, with the same
+ *     checks (pointer alignment, sinks and dsinks included) except that
+ *     args->dsum is not looked at. */
 BSA_API bsa_status bsa_bwd_noalloc(const bsa_bwd_args* args, const bsa_mask_info* fwd_info,
                                    const bsa_mask_info* dkv_info, bsa_stream stream);
 
-/* Synchronises `stream`, returns the device error word in *word (0 = none;
- * bit 1 = a bounded wait ran out, bit 2 = out-of-range MaskInfo index,
- * bit 4 = tensor-memory allocation failure) and clears it.  The status is
- * BSA_ERR_TIMEOUT / BSA_ERR_DEVICE when the word is non-zero. */
+/* Synchronises `stream`, returns the device error word of the current
+ * device in *word (0 = none; bit 1 = a bounded wait ran out, bit 2 =
+ * out-of-range MaskInfo index, bit 4 = tensor-memory allocation failure)
+ * and clears it.  The word is the OR of the library's word (set by every
+ * launch but those of bsa_bwd_noalloc) and bsa_bwd_noalloc's own; a word
+ * no launch has set up yet reads as 0, and nothing is allocated here.  The
+ * status is BSA_ERR_TIMEOUT / BSA_ERR_DEVICE when the word is non-zero. */
 BSA_API bsa_status bsa_get_device_error(bsa_stream stream, uint32_t* word);
 
 /* Time limit of one device-side wait, in nanoseconds (default 2e9).  Applies

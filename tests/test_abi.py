@@ -180,3 +180,47 @@ def test_fwd_merge_rejects_bad_arguments_on_host(kw, status):
     for k, v in kw.items():
         setattr(a, k, v)
     assert L.bsa_fwd_merge(C.byref(a), None) == getattr(_abi, status), L.bsa_last_error()
+
+
+def _bwd_args(**kw):
+    from block_sparse_attention_process_gb300 import _abi
+    a = _abi.BwdArgs(16, 32, 48, 64, 80, 96, 112, 128, 144, 160, 1, 2, 2, 128, 256, 256, math.nan, 1,
+                     0.0, 176, 192, 2, 0)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("entry", ["bsa_bwd", "bsa_bwd_noalloc"])
+@pytest.mark.parametrize("kw,status", [
+    ({"sinks": 178}, "INVALID_ARG"),     # sinks not 4-byte aligned
+    ({"dsinks": 194}, "INVALID_ARG"),    # dsinks not 4-byte aligned
+    ({"sinks": None}, "INVALID_ARG"),    # num_sinks > 0 without sinks
+    ({"num_sinks": 65}, "UNSUPPORTED"),
+    ({"logits_soft_cap": -1.0}, "INVALID_ARG"),
+    ({"dk": 8}, "INVALID_ARG"),          # misaligned tensor
+    ({"D": 96}, "UNSUPPORTED"),
+    ({"Hq": 3}, "INVALID_ARG"),
+])
+def test_backward_entry_points_reject_bad_arguments_on_host(entry, kw, status):
+    """Both backward entry points make the same host-side checks, before any
+    launch (so they run without a GPU)."""
+    ensure_built()
+    from block_sparse_attention_process_gb300 import _abi
+    L = _abi.lib()
+    a = _bwd_args(**kw)
+    fn = getattr(L, entry)
+    st = fn(C.byref(a), C.c_void_p(1), C.c_void_p(1), None)
+    assert st == getattr(_abi, status), (entry, kw, L.bsa_last_error())
+
+
+def test_noalloc_ignores_the_dsum_pointer_but_bwd_needs_it():
+    ensure_built()
+    from block_sparse_attention_process_gb300 import _abi
+    L = _abi.lib()
+    a = _bwd_args(dsum=None, num_sinks=0, sinks=None, dsinks=None)
+    assert L.bsa_bwd(C.byref(a), C.c_void_p(1), C.c_void_p(1), None) == _abi.INVALID_ARG
+    # the allocation-free entry point gets past the argument checks to the
+    # MaskInfo checks (null MaskInfo -> invalid argument, with that message)
+    assert L.bsa_bwd_noalloc(C.byref(a), None, None, None) == _abi.INVALID_ARG
+    assert b"MaskInfo" in L.bsa_last_error()

@@ -175,3 +175,84 @@ def test_full_size_sampled_heads(name, heads):
             compare(f"dQ[{b},{h}]", dq[b, h], rdq, TOL_GRAD)
         compare(f"dK[{b},{g}]", dk[b, g], rdk, TOL_GRAD)
         compare(f"dV[{b},{g}]", dv[b, g], rdv, TOL_GRAD)
+
+
+# ------------------------------------------------- the benchmarked configuration
+
+def test_small_gqa_bf16_unsplit_tensor_store_epilogue():
+    """bf16 gradients of a GQA case with enough key/value tiles (B * Hkv *
+    S/128 = 4 * 8 * 10 = 320, two per SM) that the dK/dV launch keeps each
+    q-head group in one CTA and writes bf16 dK/dV through its tensor-store
+    epilogue (the path the GQA benchmark times), compared in full."""
+    need_gpu()
+    B, Hq, Hkv, S, D = 4, 16, 8, 1280, 128
+    assert B * Hkv * (S // 128) >= 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    spec = MaskSpec("causal")
+    q, k, v, do = qkvdo(B, Hq, Hkv, S, D, seed=22)
+    dq, dk, dv, _, _ = gpu_fwd_bwd(q, k, v, do, spec, grad_fp32=False)
+    ref = oatt.backward(f64(q), f64(k), f64(v), f64(do), omask(spec, S))
+    check_grads((dq, dk, dv), ref, False)
+
+
+def _group_reference(q, k, v, do, mask, b, g, group, D):
+    """Oracle dQ of the group's q heads and the group's summed dK/dV."""
+    scale = 1 / math.sqrt(D)
+    rdk = np.zeros(k.shape[2:])
+    rdv = np.zeros(v.shape[2:])
+    rdq = {}
+    for h in range(g * group, (g + 1) * group):
+        dqh, dkh, dvh, _, _, _, _ = oatt.head_backward(f64(q[b, h]), f64(k[b, g]), f64(v[b, g]), f64(do[b, h]),
+                                                       oatt.mask_rows_for(mask, h), scale)
+        rdq[h] = dqh
+        rdk += dkh
+        rdv += dvh
+    return rdq, rdk, rdv
+
+
+def test_benchmarked_backward_bf16_gqa_causal_s8192():
+    """The backward exactly as the benchmark runs it (GQA 32/8, causal, 8192
+    tokens, D = 128, bf16 dQ/dK/dV, unsplit dK/dV with the tensor-store
+    epilogue): dK/dV of kv group 0 and dQ of its four q heads, every element,
+    against the oracle at 2e-2 plus half a bf16 ulp."""
+    need_gpu()
+    w = WORKLOADS["gqa_causal_s8192"]
+    q, k, v, do = qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed)
+    dq, dk, dv, _, _ = gpu_fwd_bwd(q, k, v, do, w.mask, grad_fp32=False)
+    group = w.Hq // w.Hkv
+    rdq, rdk, rdv = _group_reference(q, k, v, do, omask(w.mask, w.S), 0, 0, group, w.D)
+    for h, r in rdq.items():
+        compare(f"dQ[0,{h}]", dq[0, h], r, TOL_GRAD, bf16_half_ulp(r))
+    compare("dK[0,0]", dk[0, 0], rdk, TOL_GRAD, bf16_half_ulp(rdk))
+    compare("dV[0,0]", dv[0, 0], rdv, TOL_GRAD, bf16_half_ulp(rdv))
+
+
+def test_bf16_gradients_over_plain_tolerance_are_rounding_only(record_property):
+    """The forward + backward workload (B 2, H 16, causal 4096): bf16 dQ/dK/dV
+    of two sampled heads against the oracle.  Counts the elements whose error
+    exceeds the plain 2e-2 and checks that each of them sits where the bf16
+    rounding of the output is a large part of it (|x| >= 2, where half a bf16
+    ulp is 1/128 or more), and that the fp32 outputs of the same heads are within the
+    plain 2e-2 everywhere."""
+    need_gpu()
+    w = WORKLOADS["mha_causal_s4096_fwdbwd"]
+    q, k, v, do = qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed=w.seed)
+    bf = gpu_fwd_bwd(q, k, v, do, w.mask, grad_fp32=False)
+    fp = gpu_fwd_bwd(q, k, v, do, w.mask, grad_fp32=True)
+    mask = omask(w.mask, w.S)
+    total, over, worst, worst_fp32 = 0, 0, 0.0, 0.0
+    for b, h in ((0, 0), (1, 15)):
+        rdq, rdk, rdv = _group_reference(q, k, v, do, mask, b, h, 1, w.D)
+        for name, i, r in (("dQ", 0, rdq[h]), ("dK", 1, rdk), ("dV", 2, rdv)):
+            got = bf[i][b, h].astype(np.float64)
+            err = np.abs(got - r)
+            hi = err > TOL_GRAD
+            total += err.size
+            over += int(hi.sum())
+            worst = max(worst, float(err.max()))
+            assert np.all(np.abs(r[hi]) >= 2.0), f"{name}[{b},{h}]: an element over 2e-2 at |x| < 2"
+            compare(f"{name}[{b},{h}] bf16", got, r, TOL_GRAD, bf16_half_ulp(r))
+            worst_fp32 = max(worst_fp32, compare(f"{name}[{b},{h}] fp32", fp[i][b, h], r, TOL_GRAD))
+    record_property("bf16_over_2e-2", over)
+    record_property("bf16_elements", total)
+    print(f"\nbf16 gradient elements over 2e-2: {over} of {total} ({over / total:.2e}); "
+          f"max-abs bf16 {worst:.3e}, fp32 {worst_fp32:.3e}")
