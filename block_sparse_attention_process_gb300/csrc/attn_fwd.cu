@@ -668,15 +668,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!((mbits >> c) & 1ull)) xu[c] = 0xFF800000u;  // -inf
       }
       // partial row max over this part: four chains of three-input maxima
+      // (columns 0-3 start the chains, 4 .. kCols-5 in steps of eight, the
+      // last four close two of them)
+      static_assert(kCols % 8 == 0, "the max chains take columns eight at a time");
       float m0 = __uint_as_float(xu[0]), m1 = __uint_as_float(xu[1]);
       float m2 = __uint_as_float(xu[2]), m3 = __uint_as_float(xu[3]);
 #pragma unroll
-      for (int c = 4; c < kCols; c += 8) {
+      for (int c = 4; c + 8 <= kCols - 4; c += 8) {
         m0 = fmax3(m0, __uint_as_float(xu[c + 0]), __uint_as_float(xu[c + 1]));
         m1 = fmax3(m1, __uint_as_float(xu[c + 2]), __uint_as_float(xu[c + 3]));
         m2 = fmax3(m2, __uint_as_float(xu[c + 4]), __uint_as_float(xu[c + 5]));
         m3 = fmax3(m3, __uint_as_float(xu[c + 6]), __uint_as_float(xu[c + 7]));
       }
+      m0 = fmax3(m0, __uint_as_float(xu[kCols - 4]), __uint_as_float(xu[kCols - 3]));
+      m1 = fmax3(m1, __uint_as_float(xu[kCols - 2]), __uint_as_float(xu[kCols - 1]));
       const float pm = fmax3(fmaxf(m0, m1), m2, m3);
       const float mx = pm;
       // tanh is increasing: the capped maximum is the cap of the maximum

@@ -197,3 +197,28 @@ def test_wait_timeout_reports_error_instead_of_hanging():
     finally:
         bsa.set_wait_limit_ns(0)
     assert bsa.get_device_error() == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_row_with_one_visible_key_returns_its_value_row_exactly(D):
+    """Closed form: a query row that sees a single key has P = 1 on it, so
+    O is that key's value row (bf16, exactly) and LSE its scaled score.
+    Causal row 0 sees key 0 only; the scores are made negative for half of
+    the heads (Q negated) so that the row maximum is below zero there too.
+    The running maximum must be the row's true maximum for P = 1 to come
+    out exactly (a maximum taken over anything else leaves P < 1, rounded
+    to bf16, and O off by up to an ulp)."""
+    need_gpu()
+    B, Hq, Hkv, S = 2, 8, 4, 384
+    q, k, v, _ = qkvdo(B, Hq, Hkv, S, D, seed=41, with_do=False)
+    # s00 = q0 . k0 / sqrt(D): flip the sign of Q's row 0 where it is positive
+    s00 = (q[:, :, 0].float() * k[:, :, 0].float().repeat_interleave(Hq // Hkv, dim=1)).sum(-1)
+    flip = torch.ones((B, Hq), dtype=torch.bfloat16)
+    flip[:, ::2] = torch.where(s00[:, ::2] > 0, -1.0, 1.0).to(torch.bfloat16)
+    q[:, :, 0] = q[:, :, 0] * flip[..., None]
+    o, lse = run_gpu(q, k, v, MaskSpec("causal"))
+    v0 = v[:, :, 0].float().repeat_interleave(Hq // Hkv, dim=1).numpy()
+    assert np.array_equal(o[:, :, 0], v0), np.abs(o[:, :, 0] - v0).max()
+    want = (q[:, :, 0].double() * k[:, :, 0].double().repeat_interleave(Hq // Hkv, dim=1)).sum(-1) / math.sqrt(D)
+    assert (want[:, ::2] < 0).all()
+    assert np.abs(lse[:, :, 0] - want.numpy()).max() <= TOL_LSE
