@@ -294,6 +294,7 @@ def run_gpu(args):
     # ---------------------------------------------------------------- inputs (resident in HBM)
     P = Prepared(bsa, w, dev, seed_offset=rank)
     dense_compile = big_dense_compile(bsa, dev)
+    perhead_compile = perhead_dense_compile(bsa, dev)
     n_exec = P.n_exec
     f_fwd, f_bwd = flops(w, n_exec)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -396,6 +397,7 @@ def run_gpu(args):
             "mask_compile_ms": round(P.compile_ms, 3),
             "mask_compile_note": "both orientations, warm median of 3 (first, cold: %.3f ms)" % P.compile_cold_ms,
             "mask_dense_compile": dense_compile,
+            "mask_dense_perhead_compile": perhead_compile,
             "roofline": roofline,
             "sustained": sustained,
             "workloads": others,
@@ -432,6 +434,53 @@ def big_dense_compile(bsa, dev):
             "gbs": round(big_s * big_s / (ms * 1e-3) / 1e9, 1),
             "note": "whole compile (classify, dedup, next-block and shrink passes, host syncs) of a "
                     "causal-pattern byte mask; GB/s = mask bytes / compile time"}
+
+
+def perhead_dense_compile(bsa, dev, H=16, S=8192):
+    """The dense-mask compiler on per-head masks: H heads of S x S bytes
+    (1 GiB at 16 x 8192), a quarter each of scattered Bernoulli(0.1) heads
+    (every block partial and distinct), causal-pattern heads, band heads
+    |q - k| <= 700 and all-ones heads; forward orientation, warm median of
+    3.  GB/s = mask bytes / compile time."""
+    g = torch.Generator(device=dev).manual_seed(1)
+    idx = torch.arange(S, device=dev)
+    m = torch.empty((H, S, S), dtype=torch.uint8, device=dev)
+    for h in range(H):
+        k = h % 4
+        if k == 0:
+            m[h] = (torch.rand((S, S), generator=g, device=dev) < 0.1).to(torch.uint8)
+        elif k == 1:
+            m[h] = (idx[:, None] >= idx[None, :]).to(torch.uint8)
+        elif k == 2:
+            m[h] = ((idx[:, None] - idx[None, :]).abs() <= 700).to(torch.uint8)
+        else:
+            m[h] = 1
+    info = bsa.mask_compile("dense", S, S, dense=m)
+    d = info.desc()
+    info.destroy()
+    times = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        bsa.mask_compile("dense", S, S, dense=m).destroy()
+        times.append((time.perf_counter() - t0) * 1e3)
+    del m
+    ms = sorted(times)[1]
+    return {"heads": H, "S": S, "mask_bytes": H * S * S, "partial_blocks": int(d.n_partial),
+            "stack_depth": int(d.num_partial), "ms": round(ms, 3), "gbs": round(H * S * S / (ms * 1e-3) / 1e9, 1),
+            "note": "whole compile of a per-head dense mask (classify, dedup, next-block and shrink passes, "
+                    "host syncs); GB/s = mask bytes / compile time"}
+
+
+def run_mask_only(args):
+    """--mask-only: the two dense-mask compile measurements alone (also the
+    command the mask-compiler ncu captures run)."""
+    import block_sparse_attention_process_gb300 as bsa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    out = {"mask_dense_compile": big_dense_compile(bsa, dev),
+           "mask_dense_perhead_compile": perhead_dense_compile(bsa, dev)}
+    print(json.dumps(out), flush=True)
 
 
 def other_workloads(bsa, args, dev, pk, n_sms, flush, stream):
@@ -685,6 +734,7 @@ def main():
                     help="seconds of back-to-back steps timed against the sustained bf16 peak (0: off)")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mask-only", action="store_true", help="only the dense-mask compile measurements")
     ap.add_argument("--ingest-ncu", metavar="REPORT",
                     help="write profiles/traffic.json for --workload from an ncu report of this bench, then exit")
     args = ap.parse_args()
@@ -693,7 +743,9 @@ def main():
         return
     if args.warmup < 3 and args.impl == "gb300":
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.mask_only:
+        run_mask_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

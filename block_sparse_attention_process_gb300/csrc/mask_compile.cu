@@ -24,6 +24,7 @@
 // <=32767 int16, else int32).  The dkv orientation is the same on the
 // transposed mask.
 #include <algorithm>
+#include <cstdlib>
 #include <vector>
 
 #include "internal.h"
@@ -38,6 +39,7 @@ struct MaskParams {
   int32_t nR, nC;  // block rows / columns in this orientation
   int64_t q_len, kv_len, left, right, chunk;
   const uint8_t* dense;
+  uint64_t hash_mask;  // bits of the block hash kept (all; fewer only to test the dedup's collision path)
 };
 
 struct Stats {
@@ -125,41 +127,79 @@ __device__ __forceinline__ const uint8_t* dense_block_row(const MaskParams& p, i
          static_cast<size_t>(kb) * B;
 }
 
-// Dense classifier: one CTA (256 threads) per cell reads the 16 KiB block,
-// answers any()/all() and hashes the normalised 0/1 bytes (order-free sum of
-// per-word hashes, so every thread layout gives the same value).
-__global__ void __launch_bounds__(256) classify_dense(MaskParams p, int8_t* __restrict__ labels,
-                                                     uint64_t* __restrict__ hashes, int64_t n_cells) {
-  __shared__ uint64_t red[8];
-  for (int64_t cell = blockIdx.x; cell < n_cells; cell += gridDim.x) {
-    const int c = static_cast<int>(cell % p.nC);
-    const int r = static_cast<int>((cell / p.nC) % p.nR);
-    const int h = static_cast<int>(cell / (static_cast<int64_t>(p.nC) * p.nR));
-    const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
-    const uint4* src = reinterpret_cast<const uint4*>(dense_block_row(p, h, r, c, row) + half * 64);
-    bool any = false, all = true;
-    uint64_t hsum = 0;
+// The 64 visibility bits of 64 mask bytes (one bit per byte, nonzero =
+// visible): bytes that are all 0/1 skip the normalisation; the multiply
+// gathers the low bits of a word's four 0/1 bytes into one nibble.
+__device__ __forceinline__ uint64_t visibility_bits(const uint4 (&w)[4]) {
+  uint32_t x[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
+                    w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
+  uint32_t high = 0;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint4 w = __ldg(src + v);
-      const uint32_t n0 = nz_bytes(w.x), n1 = nz_bytes(w.y), n2 = nz_bytes(w.z), n3 = nz_bytes(w.w);
-      any |= (n0 | n1 | n2 | n3) != 0u;
-      all &= (n0 & n1 & n2 & n3) == 0x01010101u;
-      const uint64_t e = static_cast<uint64_t>(row) * 16 + half * 8 + v * 2;  // 8-byte word index
-      hsum += mix64((static_cast<uint64_t>(n1) << 32 | n0) ^ (e * 0x9E3779B97F4A7C15ull));
-      hsum += mix64((static_cast<uint64_t>(n3) << 32 | n2) ^ ((e + 1) * 0x9E3779B97F4A7C15ull));
+  for (int i = 0; i < 16; ++i) high |= x[i];
+  if (high & 0xFEFEFEFEu) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = nz_bytes(x[i]);
+  }
+  uint64_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bits |= static_cast<uint64_t>((x[i] * 0x08040201u) >> 24) << (4 * i);
+  return bits;
+}
+
+// Dense classifier: each CTA (256 threads) takes two cells at a time, every
+// thread loading 64 bytes (half an element row) of both before using any,
+// so that 32 KiB per CTA are in flight.  A thread reduces its bytes to 64
+// visibility bits: any() / all() of the block are warp votes on them, and
+// the block's hash is an order-free sum of mix64(bits ^ position) over the
+// threads (the same value for every thread layout).  One barrier per pair
+// of cells: every warp writes its own partials, in one of two buffers by
+// iteration parity, and two threads combine them after the barrier.
+__global__ void __launch_bounds__(256, 4) classify_dense(MaskParams p, int8_t* __restrict__ labels,
+                                                        uint64_t* __restrict__ hashes, int64_t n_cells) {
+  __shared__ uint64_t red[2][2][8];    // [buffer][cell][warp] hash partial sums
+  __shared__ uint32_t vote[2][2][8];   // [buffer][cell][warp] bit 0 any, bit 1 all
+  const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t pos_key = static_cast<uint64_t>(threadIdx.x + 1) * 0x9E3779B97F4A7C15ull;
+  int buf = 0;
+  for (int64_t cell0 = static_cast<int64_t>(blockIdx.x) * 2; cell0 < n_cells;
+       cell0 += static_cast<int64_t>(gridDim.x) * 2, buf ^= 1) {
+    uint4 w[2][4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int64_t cell = cell0 + k < n_cells ? cell0 + k : cell0;
+      const int c = static_cast<int>(cell % p.nC);
+      const int r = static_cast<int>((cell / p.nC) % p.nR);
+      const int h = static_cast<int>(cell / (static_cast<int64_t>(p.nC) * p.nR));
+      const uint4* src = reinterpret_cast<const uint4*>(dense_block_row(p, h, r, c, row) + half * 64);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) w[k][v] = __ldg(src + v);
     }
-    for (int o = 16; o > 0; o >>= 1) hsum += __shfl_xor_sync(0xffffffffu, hsum, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = hsum;
-    const int a = __syncthreads_or(any);
-    const int l = __syncthreads_and(all);
-    if (threadIdx.x == 0) {
-      uint64_t t = 0;
-      for (int i = 0; i < 8; ++i) t += red[i];
-      labels[cell] = l ? 2 : (a ? 1 : 0);
-      hashes[cell] = t;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint64_t bits = visibility_bits(w[k]);
+      uint64_t hs = mix64(bits ^ pos_key);
+      for (int o = 16; o > 0; o >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, o);
+      const bool any = __any_sync(0xffffffffu, bits != 0);
+      const bool all = __all_sync(0xffffffffu, bits == ~0ull);
+      if (lane == 0) {
+        red[buf][k][warp] = hs;
+        vote[buf][k][warp] = (any ? 1u : 0u) | (all ? 2u : 0u);
+      }
     }
     __syncthreads();
+    if (threadIdx.x < 2 && cell0 + threadIdx.x < n_cells) {
+      const int k = threadIdx.x;
+      uint64_t t = 0;
+      uint32_t any = 0, all = 2;
+      for (int i = 0; i < 8; ++i) {
+        t += red[buf][k][i];
+        any |= vote[buf][k][i] & 1u;
+        all &= vote[buf][k][i] & 2u;
+      }
+      labels[cell0 + k] = all ? 2 : (any ? 1 : 0);
+      hashes[cell0 + k] = t & p.hash_mask;
+    }
   }
 }
 
@@ -189,6 +229,15 @@ __global__ void row_pass(const int8_t* __restrict__ labels, int32_t nC, int64_t 
   atomicAdd(&st->n_full, f);
 }
 
+// ---------------------------------------------------------------- scans
+// Device-wide exclusive prefix sums in three launches: per-chunk totals
+// (chunk_sums, many CTAs), an exclusive scan of the chunk totals
+// (scan_chunk_sums, one CTA: n / 1024 values), then each chunk's own scan
+// plus its offset (chunk_write, many CTAs).  The number of elements may
+// live in device memory (an earlier kernel's count), so nothing waits for
+// the host.
+constexpr int kChunk = 1024;
+
 // Block-wide exclusive scan of one int per thread (1024 threads).
 __device__ __forceinline__ int block_excl_scan(int v, int* total) {
   __shared__ int warp_sums[32];
@@ -215,20 +264,76 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total) {
   return before + x - v;
 }
 
-// List of label-1 cells in (head, row, column) order.  One CTA of 1024.
-__global__ void __launch_bounds__(1024) compact_partial(const int8_t* __restrict__ labels, int64_t n_cells,
-                                                        int32_t* __restrict__ list, Stats* st) {
-  int base_out = 0;
-  for (int64_t base = 0; base < n_cells; base += 1024) {
-    const int64_t i = base + threadIdx.x;
-    const int f = (i < n_cells && labels[i] == 1) ? 1 : 0;
+// Element count of a scan: a host value, or one read from device memory.
+struct Count {
+  int64_t host;
+  const int32_t* dev;
+  __device__ __forceinline__ int64_t get() const { return dev ? static_cast<int64_t>(*dev) : host; }
+};
+
+template <class V>
+__global__ void __launch_bounds__(kChunk) chunk_sums(V val, Count cnt, int64_t n_chunks, int32_t* __restrict__ sums) {
+  const int64_t n = cnt.get();
+  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    const int64_t i = c * kChunk + threadIdx.x;
+    const int v = i < n ? val(i) : 0;
     int total;
-    const int ex = block_excl_scan(f, &total);
-    if (f) list[base_out + ex] = static_cast<int32_t>(i);
-    base_out += total;
+    (void)block_excl_scan(v, &total);
+    if (threadIdx.x == 0) sums[c] = total;
   }
-  if (threadIdx.x == 0) st->n1 = base_out;
 }
+
+// Exclusive scan of `n` chunk totals in place (one CTA of 1024); the grand
+// total goes to *total when it is not null.
+__global__ void __launch_bounds__(kChunk) scan_chunk_sums(int32_t* __restrict__ sums, int64_t n,
+                                                         int32_t* __restrict__ total) {
+  int run = 0;
+  for (int64_t base = 0; base < n; base += kChunk) {
+    const int64_t i = base + threadIdx.x;
+    const int v = i < n ? sums[i] : 0;
+    int t;
+    const int ex = block_excl_scan(v, &t);
+    if (i < n) sums[i] = run + ex;
+    run += t;
+  }
+  if (threadIdx.x == 0 && total) *total = run;
+}
+
+// Calls out(i, v, position) for every element, position = the exclusive
+// prefix sum of the values before i.
+template <class V, class W>
+__global__ void __launch_bounds__(kChunk) chunk_write(V val, W out, Count cnt, int64_t n_chunks,
+                                                     const int32_t* __restrict__ offs) {
+  const int64_t n = cnt.get();
+  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    const int64_t i = c * kChunk + threadIdx.x;
+    const int v = i < n ? val(i) : 0;
+    int total;
+    const int ex = block_excl_scan(v, &total);
+    if (i < n) out(i, v, offs[c] + ex);
+  }
+}
+
+// ---------------------------------------------------------------- dedup
+// Value / output functors of the scans.
+struct IsPartial {  // label-1 cells
+  const int8_t* labels;
+  __device__ __forceinline__ int operator()(int64_t i) const { return labels[i] == 1 ? 1 : 0; }
+};
+struct ListOut {  // the list of label-1 cells, in (head, row, column) order
+  int32_t* list;
+  __device__ __forceinline__ void operator()(int64_t i, int v, int pos) const {
+    if (v) list[pos] = static_cast<int32_t>(i);
+  }
+};
+struct IsNew {  // a list entry that is its own first occurrence
+  const int32_t* rep;
+  __device__ __forceinline__ int operator()(int64_t k) const { return rep[k] == k ? 1 : 0; }
+};
+struct SlotOut {  // stack slots numbered in list order
+  int32_t* new_id;
+  __device__ __forceinline__ void operator()(int64_t k, int v, int pos) const { new_id[k] = v ? pos : -1; }
+};
 
 __device__ __forceinline__ bool blocks_equal(const MaskParams& p, int64_t cell_a, int64_t cell_b, int lane) {
   const int64_t per_head = static_cast<int64_t>(p.nC) * p.nR;
@@ -247,54 +352,93 @@ __device__ __forceinline__ bool blocks_equal(const MaskParams& p, int64_t cell_a
   return __all_sync(0xffffffffu, eq);
 }
 
-// For each label-1 cell k of the list, the first list entry with the same
-// bytes (possibly k itself).  One warp per entry; hashes filter, a full byte
-// compare decides.
-__global__ void find_first_equal(MaskParams p, const int32_t* __restrict__ list, int32_t n1,
-                                 const uint64_t* __restrict__ hashes, int32_t* __restrict__ rep) {
+// Open-addressing table from a block's hash to the smallest list index
+// holding that hash.  An entry whose hash is the empty marker is stored
+// under hash ^ 1: keys only select candidates, equality is always decided
+// by comparing the bytes.
+struct HashSlot {
+  unsigned long long key;
+  unsigned int min_k;
+  unsigned int pad;
+};
+constexpr unsigned long long kEmptyKey = ~0ull;
+
+__device__ __forceinline__ unsigned long long table_key(uint64_t h) { return h == kEmptyKey ? h ^ 1ull : h; }
+
+__global__ void hash_insert(const int32_t* __restrict__ list, const uint64_t* __restrict__ hashes,
+                            const int32_t* __restrict__ n1_dev, HashSlot* __restrict__ tab, uint64_t mask) {
+  const int64_t n1 = *n1_dev;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n1;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const unsigned long long key = table_key(hashes[list[k]]);
+    uint64_t slot = (key >> 20) & mask;
+    for (uint64_t probe = 0; probe <= mask; ++probe) {  // the table has more slots than entries
+      const unsigned long long prev = atomicCAS(&tab[slot].key, kEmptyKey, key);
+      if (prev == kEmptyKey || prev == key) {
+        atomicMin(&tab[slot].min_k, static_cast<unsigned int>(k));
+        break;
+      }
+      slot = (slot + 1) & mask;
+    }
+  }
+}
+
+// For each list entry k, the first list entry with the same bytes (possibly
+// k itself): the table's smallest index with k's hash, confirmed by a byte
+// compare; a hash shared by different blocks falls back to a scan of the
+// earlier entries.  One warp per entry.
+__global__ void hash_resolve(MaskParams p, const int32_t* __restrict__ list, const uint64_t* __restrict__ hashes,
+                             const int32_t* __restrict__ n1_dev, const HashSlot* __restrict__ tab, uint64_t mask,
+                             int32_t* __restrict__ rep) {
   const int lane = threadIdx.x & 31;
+  const int64_t n1 = *n1_dev;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t k = warp_global; k < n1; k += nwarps) {
     const int32_t cell = list[k];
     const uint64_t hk = hashes[cell];
-    int32_t found = -1;
-    for (int64_t base = 0; base <= k && found < 0; base += 32) {
-      const int64_t j = base + lane;
-      const bool cand = j <= k && hashes[list[j]] == hk;
-      uint32_t m = __ballot_sync(0xffffffffu, cand);
-      while (m && found < 0) {
-        const int b = __ffs(m) - 1;
-        m &= m - 1;
-        const int64_t jj = base + b;
-        if (jj == k || blocks_equal(p, list[jj], cell, lane)) found = static_cast<int32_t>(jj);
+    const unsigned long long key = table_key(hk);
+    uint64_t slot = (key >> 20) & mask;
+    int64_t cand = k;
+    for (uint64_t probe = 0; probe <= mask; ++probe) {
+      const unsigned long long t = tab[slot].key;
+      if (t == key) {
+        cand = tab[slot].min_k;
+        break;
+      }
+      if (t == kEmptyKey) break;  // not reached: every entry was inserted
+      slot = (slot + 1) & mask;
+    }
+    int64_t found = -1;
+    if (cand >= k) {
+      found = k;
+    } else if (blocks_equal(p, list[cand], cell, lane)) {
+      found = cand;
+    } else {
+      // two different blocks with one hash: the first equal earlier entry
+      for (int64_t base = cand + 1; base <= k && found < 0; base += 32) {
+        const int64_t j = base + lane;
+        const bool c = j <= k && hashes[list[j]] == hk;
+        uint32_t m = __ballot_sync(0xffffffffu, c);
+        while (m && found < 0) {
+          const int b = __ffs(m) - 1;
+          m &= m - 1;
+          const int64_t jj = base + b;
+          if (jj == k || blocks_equal(p, list[jj], cell, lane)) found = jj;
+        }
       }
     }
-    if (lane == 0) rep[k] = found;
+    if (lane == 0) rep[k] = static_cast<int32_t>(found);
   }
-}
-
-// Stack slots: new entries numbered in list order; duplicates take their
-// first occurrence's slot.  One CTA of 1024.
-__global__ void __launch_bounds__(1024) assign_slots(const int32_t* __restrict__ rep, int32_t n1,
-                                                     int32_t* __restrict__ new_id, Stats* st) {
-  int base_out = 0;
-  for (int base = 0; base < n1; base += 1024) {
-    const int k = base + threadIdx.x;
-    const int f = (k < n1 && rep[k] == k) ? 1 : 0;
-    int total;
-    const int ex = block_excl_scan(f, &total);
-    if (k < n1) new_id[k] = f ? base_out + ex : -1;
-    base_out += total;
-  }
-  if (threadIdx.x == 0) st->P = base_out;
 }
 
 __global__ void scatter_slots(const int32_t* __restrict__ list, const int32_t* __restrict__ rep,
-                              const int32_t* __restrict__ new_id, int32_t n1, int32_t* __restrict__ slot_of_cell) {
-  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (k >= n1) return;
-  slot_of_cell[list[k]] = new_id[rep[k]];
+                              const int32_t* __restrict__ new_id, const int32_t* __restrict__ n1_dev,
+                              int32_t* __restrict__ slot_of_cell) {
+  const int64_t n1 = *n1_dev;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n1;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    slot_of_cell[list[k]] = new_id[rep[k]];
 }
 
 // The stacked blocks as bits for the attention kernels: one thread per
@@ -407,28 +551,82 @@ __global__ void iota_i32(int32_t* __restrict__ out, int64_t n) {
   if (i < n) out[i] = static_cast<int32_t>(i);
 }
 
-// Rows ordered by decreasing number of non-empty blocks (stable), for a
-// longest-first work order.  Counting sort in one CTA of 1024.
-__global__ void __launch_bounds__(1024) order_rows(const int32_t* __restrict__ row_len, int32_t n_rows,
-                                                   int32_t max_len, int32_t* __restrict__ hist,
-                                                   int32_t* __restrict__ order) {
-  for (int i = threadIdx.x; i <= max_len; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < n_rows; i += blockDim.x) atomicAdd(&hist[max_len - row_len[i]], 1);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int i = 0; i <= max_len; ++i) {
-      const int c = hist[i];
-      hist[i] = run;
-      run += c;
+// Rows ordered by decreasing number of non-empty blocks, ties by row index
+// (a stable counting sort, for a longest-first work order): bucket
+// b = max_len - row_len.  order_count counts rows per (bucket, chunk of
+// 1024 rows); an exclusive scan of those counts, bucket-major, gives each
+// (bucket, chunk) its first output position; order_place ranks each chunk's
+// rows within their bucket by a bitonic sort of (bucket, row) in shared
+// memory and writes them out.
+__global__ void order_count(const int32_t* __restrict__ row_len, int64_t n_rows, int32_t max_len, int64_t n_chunks,
+                            int32_t* __restrict__ cnt) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_rows;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    atomicAdd(&cnt[static_cast<int64_t>(max_len - row_len[i]) * n_chunks + i / kChunk], 1);
+}
+
+struct ArrayVal {
+  const int32_t* a;
+  __device__ __forceinline__ int operator()(int64_t i) const { return a[i]; }
+};
+struct ArrayOut {  // exclusive prefix sums in place of the values
+  int32_t* a;
+  __device__ __forceinline__ void operator()(int64_t i, int, int pos) const { a[i] = pos; }
+};
+
+__global__ void __launch_bounds__(kChunk) order_place(const int32_t* __restrict__ row_len, int64_t n_rows,
+                                                     int32_t max_len, int64_t n_chunks,
+                                                     const int32_t* __restrict__ offs, int32_t* __restrict__ order) {
+  __shared__ unsigned long long key[kChunk];
+  __shared__ int start[kChunk];
+  const int t = threadIdx.x;
+  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    const int64_t i = c * kChunk + t;
+    key[t] = i < n_rows ? (static_cast<unsigned long long>(max_len - row_len[i]) << 32) | static_cast<unsigned>(t)
+                        : ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= kChunk; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const int partner = t ^ j;
+        if (partner > t) {
+          const unsigned long long a = key[t], b = key[partner];
+          const bool up = (t & k) == 0;
+          if ((a > b) == up) {
+            key[t] = b;
+            key[partner] = a;
+          }
+        }
+        __syncthreads();
+      }
+    const unsigned long long me = key[t];
+    const uint32_t bucket = static_cast<uint32_t>(me >> 32);
+    start[t] = (t == 0 || static_cast<uint32_t>(key[t - 1] >> 32) != bucket) ? t : 0;
+    __syncthreads();
+    // inclusive max-scan: the first position of each thread's bucket
+    for (int o = 1; o < kChunk; o <<= 1) {
+      const int v = t >= o ? start[t - o] : 0;
+      __syncthreads();
+      if (v > start[t]) start[t] = v;
+      __syncthreads();
     }
+    if (me != ~0ull)
+      order[offs[static_cast<int64_t>(bucket) * n_chunks + c] + (t - start[t])] =
+          static_cast<int32_t>(c * kChunk + static_cast<int64_t>(me & 0xFFFFFFFFull));
+    __syncthreads();
   }
-  __syncthreads();
-  // stable placement: one thread walks the rows in order
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < n_rows; ++i) order[hist[max_len - row_len[i]]++] = i;
-  }
+}
+
+// BSA_DEDUP_HASH_BITS=n (0..63) keeps only the low n bits of every block
+// hash, so that different blocks share hashes and the dedup has to settle
+// them by comparing bytes (for testing that path; the default keeps all 64).
+uint64_t dedup_hash_mask() {
+  static const uint64_t m = [] {
+    const char* e = std::getenv("BSA_DEDUP_HASH_BITS");
+    if (!e || !*e) return ~0ull;
+    const int n = std::atoi(e);
+    return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1));
+  }();
+  return m;
 }
 
 int idx_bytes(int64_t max_value) {
@@ -462,6 +660,7 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   p.right = spec->local_right;
   p.chunk = spec->chunk;
   p.dense = spec->dense;
+  p.hash_mask = dedup_hash_mask();
   const int nq = static_cast<int>(spec->q_len / B), nk = static_cast<int>(spec->kv_len / B);
   p.nR = p.orient == BSA_ORIENT_FWD ? nq : nk;
   p.nC = p.orient == BSA_ORIENT_FWD ? nk : nq;
@@ -471,7 +670,7 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   const bool dense = p.kind == BSA_MASK_DENSE;
 
   DevBuf labels(stream), hashes(stream), stats(stream), list(stream), rep(stream), new_id(stream),
-      slot_of_cell(stream), hist(stream);
+      slot_of_cell(stream), hist(stream), csum(stream), csum2(stream), table(stream);
   cudaError_t e;
 #define BSA_CK(x, what)                         \
   do {                                          \
@@ -529,35 +728,56 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   row_pass<<<static_cast<unsigned>((n_rows + 127) / 128), 128, 0, stream>>>(
       static_cast<int8_t*>(labels.p), p.nC, n_rows, info->row_len, st);
   BSA_CK(cudaGetLastError(), "row_pass launch");
+  const int64_t n_chunks = (n_cells + kChunk - 1) / kChunk;
+  const unsigned scan_grid = static_cast<unsigned>(std::min<int64_t>(n_chunks, 152 * 8));
   if (dense) {
+    // list of the label-1 cells (its length n1 stays on the device)
     BSA_ALLOC(list.p, n_cells * sizeof(int32_t));
-    compact_partial<<<1, 1024, 0, stream>>>(static_cast<int8_t*>(labels.p), n_cells,
-                                            static_cast<int32_t*>(list.p), st);
+    BSA_ALLOC(csum.p, n_chunks * sizeof(int32_t));
+    int32_t* lst = static_cast<int32_t*>(list.p);
+    int32_t* cs = static_cast<int32_t*>(csum.p);
+    const IsPartial is_partial{static_cast<int8_t*>(labels.p)};
+    const Count all_cells{n_cells, nullptr};
+    chunk_sums<<<scan_grid, kChunk, 0, stream>>>(is_partial, all_cells, n_chunks, cs);
+    scan_chunk_sums<<<1, kChunk, 0, stream>>>(cs, n_chunks, &st->n1);
+    chunk_write<<<scan_grid, kChunk, 0, stream>>>(is_partial, ListOut{lst}, all_cells, n_chunks, cs);
     BSA_CK(cudaGetLastError(), "compact launch");
+    // first occurrence of each partial block: hash table, then byte compare
+    uint64_t tab_n = 64;
+    while (tab_n < 2 * static_cast<uint64_t>(n_cells)) tab_n <<= 1;
+    BSA_ALLOC(table.p, tab_n * sizeof(HashSlot));
+    BSA_CK(cudaMemsetAsync(table.p, 0xFF, tab_n * sizeof(HashSlot), stream), "clear hash table");
+    BSA_ALLOC(rep.p, n_cells * sizeof(int32_t));
+    BSA_ALLOC(new_id.p, n_cells * sizeof(int32_t));
+    BSA_ALLOC(slot_of_cell.p, n_cells * sizeof(int32_t));
+    const int32_t* n1_dev = &st->n1;
+    const uint64_t* hsh = static_cast<uint64_t*>(hashes.p);
+    HashSlot* tab = static_cast<HashSlot*>(table.p);
+    int32_t* rp = static_cast<int32_t*>(rep.p);
+    int32_t* nid = static_cast<int32_t*>(new_id.p);
+    hash_insert<<<static_cast<unsigned>(std::min<int64_t>((n_cells + 255) / 256, 152 * 16)), 256, 0, stream>>>(
+        lst, hsh, n1_dev, tab, tab_n - 1);
+    hash_resolve<<<static_cast<unsigned>(std::min<int64_t>((n_cells + 7) / 8, 152 * 16)), 256, 0, stream>>>(
+        p, lst, hsh, n1_dev, tab, tab_n - 1, rp);
+    BSA_CK(cudaGetLastError(), "dedup launch");
+    // stack slots: new blocks numbered in list order, duplicates take their
+    // first occurrence's slot
+    const IsNew is_new{rp};
+    const Count n1_count{0, n1_dev};
+    chunk_sums<<<scan_grid, kChunk, 0, stream>>>(is_new, n1_count, n_chunks, cs);
+    scan_chunk_sums<<<1, kChunk, 0, stream>>>(cs, n_chunks, &st->P);
+    chunk_write<<<scan_grid, kChunk, 0, stream>>>(is_new, SlotOut{nid}, n1_count, n_chunks, cs);
+    scatter_slots<<<static_cast<unsigned>(std::min<int64_t>((n_cells + 255) / 256, 152 * 16)), 256, 0, stream>>>(
+        lst, rp, nid, n1_dev, static_cast<int32_t*>(slot_of_cell.p));
+    BSA_CK(cudaGetLastError(), "slots launch");
   }
+  // one synchronisation: the grid width, the largest column, the counts
+  // and the stack depth size the MaskInfo arrays
   Stats hs{};
   BSA_CK(cudaMemcpyAsync(&hs, st, sizeof(Stats), cudaMemcpyDeviceToHost, stream), "read stats");
   BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
 
   if (dense && hs.n1 > 0) {
-    BSA_ALLOC(rep.p, hs.n1 * sizeof(int32_t));
-    BSA_ALLOC(new_id.p, hs.n1 * sizeof(int32_t));
-    BSA_ALLOC(slot_of_cell.p, n_cells * sizeof(int32_t));
-    const int warps_per_cta = 8;
-    const int ctas = static_cast<int>(std::min<int64_t>((hs.n1 + warps_per_cta - 1) / warps_per_cta, 152 * 16));
-    find_first_equal<<<ctas, 32 * warps_per_cta, 0, stream>>>(p, static_cast<int32_t*>(list.p), hs.n1,
-                                                              static_cast<uint64_t*>(hashes.p),
-                                                              static_cast<int32_t*>(rep.p));
-    BSA_CK(cudaGetLastError(), "dedup launch");
-    assign_slots<<<1, 1024, 0, stream>>>(static_cast<int32_t*>(rep.p), hs.n1, static_cast<int32_t*>(new_id.p), st);
-    BSA_CK(cudaGetLastError(), "slots launch");
-    scatter_slots<<<(hs.n1 + 255) / 256, 256, 0, stream>>>(static_cast<int32_t*>(list.p),
-                                                           static_cast<int32_t*>(rep.p),
-                                                           static_cast<int32_t*>(new_id.p), hs.n1,
-                                                           static_cast<int32_t*>(slot_of_cell.p));
-    BSA_CK(cudaGetLastError(), "scatter launch");
-    BSA_CK(cudaMemcpyAsync(&hs.P, &st->P, sizeof(int32_t), cudaMemcpyDeviceToHost, stream), "read P");
-    BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
     BSA_ALLOC(info->partial, static_cast<size_t>(hs.P) * B * B);
     copy_stack<<<static_cast<unsigned>(std::min<int64_t>(hs.n1, 152 * 16)), 256, 0, stream>>>(
         p, static_cast<int32_t*>(list.p), static_cast<int32_t*>(new_id.p), hs.n1, info->partial);
@@ -586,10 +806,6 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   BSA_ALLOC(info->block_mask, alloc_n);
   BSA_ALLOC(info->data_next, alloc_n * info->data_next_bytes);
   if (dense) BSA_ALLOC(info->mask_next, alloc_n * info->mask_next_bytes);
-  if (dense && !slot_of_cell.p) {
-    BSA_ALLOC(slot_of_cell.p, n_cells * sizeof(int32_t));
-    BSA_CK(cudaMemsetAsync(slot_of_cell.p, 0, n_cells * sizeof(int32_t), stream), "clear slots");
-  }
   if (n_out) {
     write_rows<<<static_cast<unsigned>((n_rows + 127) / 128), 128, 0, stream>>>(
         static_cast<int8_t*>(labels.p), static_cast<int32_t*>(slot_of_cell.p), p.nC, n_rows, width, opts->shrink,
@@ -598,10 +814,26 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   }
   iota_i32<<<static_cast<unsigned>((p.q_len + 255) / 256), 256, 0, stream>>>(info->q_sequence, p.q_len);
   BSA_CK(cudaGetLastError(), "iota launch");
-  BSA_ALLOC(hist.p, (p.nC + 1) * sizeof(int32_t));
-  order_rows<<<1, 1024, 0, stream>>>(info->row_len, static_cast<int32_t>(n_rows), p.nC,
-                                     static_cast<int32_t*>(hist.p), info->row_order);
-  BSA_CK(cudaGetLastError(), "order_rows launch");
+  // rows by decreasing length (stable counting sort)
+  {
+    const int64_t r_chunks = (n_rows + kChunk - 1) / kChunk;
+    const int64_t n_cnt = static_cast<int64_t>(p.nC + 1) * r_chunks;
+    BSA_ALLOC(hist.p, n_cnt * sizeof(int32_t));
+    int32_t* cnt = static_cast<int32_t*>(hist.p);
+    BSA_CK(cudaMemsetAsync(cnt, 0, n_cnt * sizeof(int32_t), stream), "clear row counts");
+    order_count<<<static_cast<unsigned>(std::min<int64_t>((n_rows + 255) / 256, 152 * 16)), 256, 0, stream>>>(
+        info->row_len, n_rows, p.nC, r_chunks, cnt);
+    const int64_t c_chunks = (n_cnt + kChunk - 1) / kChunk;
+    BSA_ALLOC(csum2.p, c_chunks * sizeof(int32_t));
+    int32_t* cs2 = static_cast<int32_t*>(csum2.p);
+    const unsigned g2 = static_cast<unsigned>(std::min<int64_t>(c_chunks, 152 * 8));
+    chunk_sums<<<g2, kChunk, 0, stream>>>(ArrayVal{cnt}, Count{n_cnt, nullptr}, c_chunks, cs2);
+    scan_chunk_sums<<<1, kChunk, 0, stream>>>(cs2, c_chunks, nullptr);
+    chunk_write<<<g2, kChunk, 0, stream>>>(ArrayVal{cnt}, ArrayOut{cnt}, Count{n_cnt, nullptr}, c_chunks, cs2);
+    order_place<<<static_cast<unsigned>(std::min<int64_t>(r_chunks, 152 * 8)), kChunk, 0, stream>>>(
+        info->row_len, n_rows, p.nC, r_chunks, cnt, info->row_order);
+    BSA_CK(cudaGetLastError(), "row order launch");
+  }
   // host copies of the row lengths and order (for launch-time tile
   // schedules), in stream order, then one synchronisation: a returned
   // MaskInfo is complete

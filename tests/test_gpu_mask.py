@@ -139,3 +139,87 @@ def test_compile_is_deterministic():
     b = bsa.mask_compile("dense", 640, 640, dense=dense).to_host()
     for k in ("block_mask", "data_next", "mask_next", "partial_mask_blocks"):
         assert np.array_equal(a[k], b[k])
+
+
+def per_head_dense_mask(H, S, seed=0):
+    """[H, S, S] uint8 with four kinds of heads: scattered Bernoulli(0.1)
+    (every block partial and distinct), a causal pattern (all diagonal
+    blocks partial and equal, shared across heads), planted blocks (zeros,
+    ones, three repeated patterns, fresh random ones) and a band
+    |q - k| <= 700 (repeating partial edge blocks)."""
+    m = np.zeros((H, S, S), np.uint8)
+    idx = np.arange(S)
+    for h in range(H):
+        kind = h % 4
+        if kind == 0:
+            m[h] = bernoulli_mask(S, 0.1, seed + h)
+        elif kind == 1:
+            m[h] = idx[:, None] >= idx[None, :]
+        elif kind == 2:
+            m[h] = planted_block_mask(1, S // 128, S // 128, seed=seed + h)[0]
+        else:
+            m[h] = np.abs(idx[:, None] - idx[None, :]) <= 700
+    return m
+
+
+@pytest.mark.parametrize("orientation", ["fwd", "dkv"])
+def test_per_head_dense_mask_s8192_bit_exact(orientation):
+    """Sixteen mask heads of 8192 x 8192 (1 GiB of mask bytes, 65536 blocks,
+    tens of thousands partial): every MaskInfo array against the oracle."""
+    need_gpu()
+    H, S = 16, 8192
+    m = per_head_dense_mask(H, S)
+    ref, got = compile_both("dense", S, S, dense=m, orientation=orientation)
+    assert got["heads"] == H
+    assert_same(ref, got)
+
+
+@pytest.mark.parametrize("bits", [0, 3])
+def test_dedup_settles_shared_hashes_by_bytes(bits, tmp_path):
+    """With the block hashes cut to `bits` bits (BSA_DEDUP_HASH_BITS, read
+    when the library is loaded, hence a child process) different partial
+    blocks share hashes; the first-occurrence search must still pick the
+    first block with equal bytes."""
+    need_gpu()
+    import os
+    import subprocess
+    import sys
+    from helpers import ROOT
+    script = r'''
+import sys, numpy as np, torch
+sys.path.insert(0, ROOT); sys.path.insert(0, ROOT + "/tests")
+from test_gpu_mask import compile_both, assert_same
+from workloads import planted_block_mask, bernoulli_mask
+for seed in (0, 1):
+    m = planted_block_mask(3, 5, 7, seed=seed)
+    for o in ("fwd", "dkv"):
+        assert_same(*compile_both("dense", 5 * 128, 7 * 128, dense=m, orientation=o))
+m = np.stack([bernoulli_mask(1024, 0.2, 9)] * 2)
+assert_same(*compile_both("dense", 1024, 1024, dense=m))
+print("ok")
+'''.replace("ROOT", repr(ROOT))
+    env = dict(os.environ, BSA_DEDUP_HASH_BITS=str(bits))
+    r = subprocess.run([sys.executable, "-c", script], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+def test_many_partial_blocks_with_duplicates_across_chunks():
+    """More than a thousand partial blocks (the list, the slot numbering and
+    the row order each span several 1024-entry chunks), many of them
+    repeated across rows and heads."""
+    need_gpu()
+    H, nq, nk = 4, 24, 24
+    rng = np.random.default_rng(5)
+    pats = [(rng.random((128, 128)) < 0.5).astype(np.uint8) for _ in range(40)]
+    m = np.zeros((H, nq * 128, nk * 128), np.uint8)
+    for h in range(H):
+        for i in range(nq):
+            for j in range(nk):
+                r = rng.random()
+                blk = pats[int(rng.integers(0, 40))] if r < 0.7 else (
+                    np.ones((128, 128), np.uint8) if r < 0.8 else np.zeros((128, 128), np.uint8))
+                m[h, i * 128:(i + 1) * 128, j * 128:(j + 1) * 128] = blk
+    for o in ("fwd", "dkv"):
+        ref, got = compile_both("dense", nq * 128, nk * 128, dense=m, orientation=o)
+        assert ref.n_partial > 1024 and got["num_partial"] == 40
+        assert_same(ref, got)
