@@ -293,8 +293,8 @@ def run_gpu(args):
 
     # ---------------------------------------------------------------- inputs (resident in HBM)
     P = Prepared(bsa, w, dev, seed_offset=rank)
-    dense_compile = big_dense_compile(bsa, dev)
-    perhead_compile = perhead_dense_compile(bsa, dev)
+    dense_compile = None if args.no_mask_bench else big_dense_compile(bsa, dev)
+    perhead_compile = None if args.no_mask_bench else perhead_dense_compile(bsa, dev)
     n_exec = P.n_exec
     f_fwd, f_bwd = flops(w, n_exec)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -735,6 +735,8 @@ def main():
     ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mask-only", action="store_true", help="only the dense-mask compile measurements")
+    ap.add_argument("--no-mask-bench", action="store_true",
+                    help="skip the large dense-mask compile measurements (shorter runs for profiling)")
     ap.add_argument("--ingest-ncu", metavar="REPORT",
                     help="write profiles/traffic.json for --workload from an ncu report of this bench, then exit")
     args = ap.parse_args()
