@@ -25,7 +25,7 @@ from ._abi import BsaError, check
 
 __all__ = ["mask_compile", "MaskInfo", "fwd", "fwd_partial", "fwd_merge", "bwd", "bwd_noalloc", "bwd_rowsum",
            "bwd_dkv", "bwd_dq",
-           "get_device_error", "set_wait_limit_ns", "debug_wait_timeout", "version", "BsaError",
+           "get_device_error", "set_wait_limit_ns", "debug_wait_timeout", "debug_selfcheck", "version", "BsaError",
            "library_path"]
 
 _KINDS = {"dense": _abi.MASK_DENSE, "causal": _abi.MASK_CAUSAL, "local": _abi.MASK_LOCAL,
@@ -319,3 +319,9 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def debug_wait_timeout(stream=None) -> None:
     check(_abi.lib().bsa_debug_wait_timeout(_stream(stream)), "bsa_debug_wait_timeout")
+
+
+def debug_selfcheck(stream=None) -> None:
+    """bsa_debug_selfcheck: out-of-range indices through the range checks
+    (recorded only by the range-checked build)."""
+    check(_abi.lib().bsa_debug_selfcheck(_stream(stream)), "bsa_debug_selfcheck")

@@ -10,7 +10,9 @@ import ctypes as C
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_lib", "libbsa.so")
+# BSA_LIBRARY_VARIANT=debug loads the range-checked build (see build.py)
+LIB_PATH = os.path.join(HERE, "_lib", "libbsa_debug.so" if os.environ.get("BSA_LIBRARY_VARIANT") == "debug"
+                        else "libbsa.so")
 
 # status codes
 OK, INVALID_ARG, UNSUPPORTED, CUDA, OOM, TIMEOUT, DEVICE = range(7)
@@ -86,6 +88,7 @@ SIGNATURES = {
     "bsa_get_device_error": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint32)]),
     "bsa_set_wait_limit_ns": (C.c_int, [C.c_uint64]),
     "bsa_debug_wait_timeout": (C.c_int, [C.c_void_p]),
+    "bsa_debug_selfcheck": (C.c_int, [C.c_void_p]),
     "bsa_status_string": (C.c_char_p, [C.c_int]),
     "bsa_last_error": (C.c_char_p, []),
     "bsa_version": (C.c_char_p, []),

@@ -142,6 +142,23 @@ __global__ void debug_wait_timeout_kernel(uint32_t* err, uint64_t limit_ns) {
   if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, w);
 }
 
+// Out-of-range indices passed through the range checks (and used for
+// nothing else): the range-checked build records DEV_ERR_DEBUG with the
+// line of the first; the release build compiles the checks away.
+__global__ void debug_selfcheck_kernel(uint32_t* err, uint32_t col, int64_t row) {
+  (void)BSA_TMEM(col, 32u, err);
+  (void)BSA_RANGE(row, int64_t(0), int64_t(16), err);
+}
+
+bsa_status debug_selfcheck_launch(cudaStream_t stream) {
+  uint32_t* err = device_error_word();
+  if (!err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
+  debug_selfcheck_kernel<<<1, 1, 0, stream>>>(err, 500u, int64_t(-1));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "debug_selfcheck launch");
+  return BSA_OK;
+}
+
 bsa_status debug_wait_timeout_launch(cudaStream_t stream) {
   uint32_t* err = device_error_word();
   if (!err) return fail(BSA_ERR_CUDA, "could not allocate the device error word");
@@ -241,6 +258,10 @@ bsa_status bsa_set_wait_limit_ns(uint64_t ns) {
 
 bsa_status bsa_debug_wait_timeout(bsa_stream stream) {
   return debug_wait_timeout_launch(static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_debug_selfcheck(bsa_stream stream) {
+  return debug_selfcheck_launch(static_cast<cudaStream_t>(stream));
 }
 
 bsa_status bsa_get_device_error(bsa_stream stream, uint32_t* word) {

@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-        mma_ss_elect(tmem + kDqColS + (n & 1u) * 128, qdesc + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss_elect(BSA_TMEM(tmem + kDqColS + (n & 1u) * 128, 128u, p.err), qdesc + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.s_full[n & 1u]);
       ++s_cnt;
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-        mma_ss_elect(tmem + kDqColDP, dodesc + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss_elect(BSA_TMEM(tmem + kDqColDP, 128u, p.err), dodesc + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.dp_full);
       mma_commit_elect(&s.v_empty[vs]);
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
       const uint64_t kmn = kmn0 + (n % kDqStagesK) * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_elect(tmem + kDqColQ, tmem + kDqColDP + part_a_col<DqShape<D>::kCols>(kk),
+        mma_ts_elect(BSA_TMEM(tmem + kDqColQ, 128u, p.err), BSA_TMEM(tmem + kDqColDP + part_a_col<DqShape<D>::kCols>(kk), 8u, p.err),
                      kmn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
       mma_commit_elect(&s.k_empty[n % kDqStagesK]);
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
         // row statistics arrive with the tile's Q/dO; q_sequence is consecutive within a block
-        qrow = static_cast<int64_t>(bi.w) + r;
+        qrow = BSA_RANGE(static_cast<int64_t>(bi.w) + r, int64_t(0), static_cast<int64_t>(p.B) * p.Hq * p.Sq, p.err);
         if (!dense_mask<kM>(p.mi.kind))
           key_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(static_cast<int32_t>(bi.z)) + r,
                        lo, hi);
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
       tc_fence_after();
       uint32_t sv[kCols];
 #pragma unroll
-      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDqColS + sb * 128 + col0 + c + lane_off, sv + c);
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(BSA_TMEM(tmem + kDqColS + sb * 128 + col0 + c + lane_off, 32u, p.err), sv + c);
       tmem_wait_ld();
       reg_fence<kCols>(sv);
       // P = exp2(s * scale_log2 - lse2), packed pairs
@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
       tc_fence_after();
       uint32_t dpv[kCols];
 #pragma unroll
-      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDqColDP + col0 + c + lane_off, dpv + c);
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(BSA_TMEM(tmem + kDqColDP + col0 + c + lane_off, 32u, p.err), dpv + c);
       tmem_wait_ld();
       reg_fence<kCols>(dpv);
       // dS = P * (dP - Dsum)
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
                   d0, d1);
         dspk[c] = pack_bf16x2(d0, d1);
       }
-      tmem_st_cols<kCols / 2>(tmem + kDqColDP + col0 + lane_off, dspk);
+      tmem_st_cols<kCols / 2>(BSA_TMEM(tmem + kDqColDP + col0 + lane_off, static_cast<uint32_t>(kCols / 2), p.err), dspk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.ds_full);
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kPartD / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + kDqColQ + part * kPartD + c * 32 + lane_off, v);
+        tmem_ld32(BSA_TMEM(tmem + kDqColQ + part * kPartD + c * 32 + lane_off, 32u, p.err), v);
         tmem_wait_ld();
         reg_fence32(v);
         store_row_wide(p.dq, p.grad_fp32, qrow, D, v, part * kPartD + c * 32, p.scale);
@@ -1009,7 +1009,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-        mma_ss_elect(tmem + kDkvColST, kdesc + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss_elect(BSA_TMEM(tmem + kDkvColST, 128u, p.err), kdesc + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.st_full);
       // K is read by the S^T MMAs only
@@ -1025,7 +1025,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-        mma_ss_elect(tmem + kDkvColDP, vdesc + off, dod + off, idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss_elect(BSA_TMEM(tmem + kDkvColDP, 128u, p.err), vdesc + off, dod + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.dpt_full);
       // V is read by the dP^T MMAs only
@@ -1063,7 +1063,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             if ((kk % kSteps) / (kSteps / 2) != h) continue;
-            mma_ts_elect(tmem + kDkvColDV, tmem + kDkvColST + part_a_col<DkvShape<D>::kCols>(kk),
+            mma_ts_elect(BSA_TMEM(tmem + kDkvColDV, 128u, p.err), BSA_TMEM(tmem + kDkvColST + part_a_col<DkvShape<D>::kCols>(kk), 8u, p.err),
                          domn + static_cast<uint64_t>(kk * 2048 >> 4), idesc_acc, (first && kk == 0) ? 0u : 1u);
           }
         }
@@ -1080,7 +1080,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       const uint64_t qmn = qmn0 + st * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_elect(tmem + kDkvColDK, tmem + kDkvColDP + part_a_col<DkvShape<D>::kCols>(kk),
+        mma_ts_elect(BSA_TMEM(tmem + kDkvColDK, 128u, p.err), BSA_TMEM(tmem + kDkvColDP + part_a_col<DkvShape<D>::kCols>(kk), 8u, p.err),
                      qmn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
       mma_commit_elect(&s.in_empty[st]);
@@ -1140,7 +1140,8 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
-        krow = static_cast<int64_t>(bi.w) + r;
+        krow = BSA_RANGE(static_cast<int64_t>(bi.w) + r, int64_t(0),
+                         (p.kv_splits > 1 ? p.kv_splits : 1) * static_cast<int64_t>(p.B) * p.Hkv * p.Skv, p.err);
         if (!dense_mask<kM>(p.mi.kind))
           query_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(bi.z) + r, lo, hi);
       }
@@ -1160,7 +1161,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       tc_fence_after();
       uint32_t sv[kCols];
 #pragma unroll
-      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + kDkvColST + col0 + c + lane_off, sv + c);
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(BSA_TMEM(tmem + kDkvColST + col0 + c + lane_off, 32u, p.err), sv + c);
       tmem_wait_ld();
       reg_fence<kCols>(sv);
       // P = exp2((s*scale - LSE) * log2e): (LSE - s*scale) then times -log2e, packed pairs
@@ -1197,7 +1198,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kCols / 4; ++c)
             ppk[c] = pack_bf16x2(pv[h * kCols / 2 + 2 * c], pv[h * kCols / 2 + 2 * c + 1]);
-          tmem_st_cols<kCols / 4>(tmem + kDkvColST + col0 + h * (kCols / 4) + lane_off, ppk);
+          tmem_st_cols<kCols / 4>(BSA_TMEM(tmem + kDkvColST + col0 + h * (kCols / 4) + lane_off, static_cast<uint32_t>(kCols / 4), p.err), ppk);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&s.p_full[h]);
@@ -1220,7 +1221,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           pv[c] = p0 * fmaf(-t0, t0, 1.f);
           pv[c + 1] = p1 * fmaf(-t1, t1, 1.f);
         }
-        tmem_st_cols<kCols / 2>(tmem + kDkvColST + col0 + lane_off, ppk);
+        tmem_st_cols<kCols / 2>(BSA_TMEM(tmem + kDkvColST + col0 + lane_off, static_cast<uint32_t>(kCols / 2), p.err), ppk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&s.p_full[0]);
@@ -1233,7 +1234,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
 #pragma unroll
       for (int h2 = 0; h2 < kCols / 32; ++h2) {  // 32 columns at a time to bound register use
         uint32_t dpv[32];
-        tmem_ld32(tmem + kDkvColDP + col0 + h2 * 32 + lane_off, dpv);
+        tmem_ld32(BSA_TMEM(tmem + kDkvColDP + col0 + h2 * 32 + lane_off, 32u, p.err), dpv);
         tmem_wait_ld();
         reg_fence32(dpv);
 #pragma unroll
@@ -1252,7 +1253,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           dspk[c / 2 + 1] = pack_bf16x2(a2, a3);
         }
       }
-      tmem_st_cols<kCols / 2>(tmem + kDkvColDP + col0 + lane_off, dspk);
+      tmem_st_cols<kCols / 2>(BSA_TMEM(tmem + kDkvColDP + col0 + lane_off, static_cast<uint32_t>(kCols / 2), p.err), dspk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.ds_full);
@@ -1269,11 +1270,11 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         uint8_t* stv = s.dout[st] + (warp - 4) * 2048;
         uint8_t* stk = s.q[st] + (warp - 4) * 2048;
         uint32_t v[32];
-        tmem_ld32(tmem + kDkvColDV + part * kPartD + lane_off, v);
+        tmem_ld32(BSA_TMEM(tmem + kDkvColDV + part * kPartD + lane_off, 32u, p.err), v);
         tmem_wait_ld();
         reg_fence32(v);
         stage_row_sw64(stv, lane, v, 1.f);
-        tmem_ld32(tmem + kDkvColDK + part * kPartD + lane_off, v);
+        tmem_ld32(BSA_TMEM(tmem + kDkvColDK + part * kPartD + lane_off, 32u, p.err), v);
         tmem_wait_ld();
         reg_fence32(v);
         stage_row_sw64(stk, lane, v, p.scale);
@@ -1292,11 +1293,11 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         __syncwarp();
       } else {
         uint32_t v[32];
-        tmem_ld32(tmem + kDkvColDV + part * kPartD + lane_off, v);
+        tmem_ld32(BSA_TMEM(tmem + kDkvColDV + part * kPartD + lane_off, 32u, p.err), v);
         tmem_wait_ld();
         reg_fence32(v);
         store_row(sp ? p.part_dv : p.dv, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD, 1.f);
-        tmem_ld32(tmem + kDkvColDK + part * kPartD + lane_off, v);
+        tmem_ld32(BSA_TMEM(tmem + kDkvColDK + part * kPartD + lane_off, 32u, p.err), v);
         tmem_wait_ld();
         reg_fence32(v);
         store_row(sp ? p.part_dk : p.dk, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD, p.scale);

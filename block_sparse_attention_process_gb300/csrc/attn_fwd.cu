@@ -228,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t t_b = te.z / p.Hq, t_hq = te.z % p.Hq;
       const int32_t t_hm = p.mi.heads == 1 ? 0 : t_hq;
       const int64_t t_row_base = (static_cast<int64_t>(t_hm) * p.mi.rows + t_i) * p.mi.width;
-      const int64_t out_row = static_cast<int64_t>(te.z) * p.Sq + static_cast<int64_t>(t_i) * 128;
+      const int64_t n_rows_q = static_cast<int64_t>(p.B) * p.Hq * p.Sq;
+      const int64_t out_row =
+          BSA_RANGE(static_cast<int64_t>(te.z) * p.Sq + static_cast<int64_t>(t_i) * 128, int64_t(0), n_rows_q - 127, p.err);
       // blocks of this launch's key range: the whole row, or (a key shard)
       // those found by a first pass over the row
       const bool ranged = p.kv_lo > 0 || p.kv_hi < p.mi.cols;
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-        mma_ss_elect(tmem + sb * 128, cur_q + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss_elect(BSA_TMEM(tmem + sb * 128, 128u, p.err), cur_q + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit_elect(&s.s_full[sb]);
       mma_commit_elect(&s.k_empty[ks]);
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // buffer) into part p's accumulator
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_elect(tmem + kTmemO + (kk >> 2) * 128, tmem + pb * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+        mma_ts_elect(BSA_TMEM(tmem + kTmemO + (kk >> 2) * 128, 128u, p.err), BSA_TMEM(tmem + pb * 128 + (kk >> 2) * 64 + (kk & 3) * 8, 8u, p.err),
                      vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_o, (pv_first && (kk & 3) == 0) ? 0u : 1u);
       mma_commit_elect(&s.v_empty[vs]);
       mma_commit_elect(&s.pv_done[pb]);
@@ -486,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
       // per-part factors of the output: normalised (bf16 O) or not (a shard's accumulator)
       const float c0 = p.partial ? w0 : w0 * inv_l, c1 = p.partial ? w1 : w1 * inv_l;
-      const int64_t orow = static_cast<int64_t>(row0) + r;
+      const int64_t orow =
+          BSA_RANGE(static_cast<int64_t>(row0) + r, int64_t(0), static_cast<int64_t>(p.B) * p.Hq * p.Sq, p.err);
       if (p.partial) {
         // (a key shard) the unnormalised fp32 accumulator w0 O_0 + w1 O_1 (for
         // the reference maximum M), 16 columns at a time
@@ -494,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
           uint32_t va[16], vb[16];
-          tmem_ld16(obase + c * 16, va);
-          tmem_ld16(obase + 128 + c * 16, vb);
+          tmem_ld16(BSA_TMEM(obase + c * 16, 16u, p.err), va);
+          tmem_ld16(BSA_TMEM(obase + 128 + c * 16, 16u, p.err), vb);
           tmem_wait_ld();
           reg_fence16(va);
           reg_fence16(vb);
@@ -522,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t va[16], vb[16];
-            tmem_ld16(obase + h * 64 + c * 16, va);
-            tmem_ld16(obase + 128 + h * 64 + c * 16, vb);
+            tmem_ld16(BSA_TMEM(obase + h * 64 + c * 16, 16u, p.err), va);
+            tmem_ld16(BSA_TMEM(obase + 128 + h * 64 + c * 16, 16u, p.err), vb);
             tmem_wait_ld();
             reg_fence16(va);
             reg_fence16(vb);
@@ -659,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t xu[kCols];
 #pragma unroll
-      for (int c = 0; c < kCols; c += 32) tmem_ld32(tmem + sb * 128 + col0 + c + lane_off, xu + c);
+      for (int c = 0; c < kCols; c += 32) tmem_ld32(BSA_TMEM(tmem + sb * 128 + col0 + c + lane_off, 32u, p.err), xu + c);
       tmem_wait_ld();
       reg_fence<kCols>(xu);
       if (label == 1) {
@@ -734,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // words [part*kCols, part*kCols + kCols/2) of the buffer.
 #pragma unroll
       for (int c = 0; c < kCols / 2; c += 16)
-        tmem_st16(tmem + sb * 128 + static_cast<uint32_t>(part) * kCols + c + lane_off, pk + c);
+        tmem_st16(BSA_TMEM(tmem + sb * 128 + static_cast<uint32_t>(part) * kCols + c + lane_off, 16u, p.err), pk + c);
       // O holds earlier blocks' sum only after the first block; rescale this
       // part's accumulator (after the previous P V has landed) when its max moved.
       if (warp_switch && exec > 0) {
@@ -746,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < D; c += 16) {
           uint32_t ov[16];
           const uint32_t oa = tmem + ocol0 + c + lane_off;
-          tmem_ld16(oa, ov);
+          tmem_ld16(BSA_TMEM(oa, 16u, p.err), ov);
           tmem_wait_ld();
           reg_fence16(ov);
 #pragma unroll
@@ -757,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ov[e] = __float_as_uint(a0);
             ov[e + 1] = __float_as_uint(a1);
           }
-          tmem_st16(oa, ov);
+          tmem_st16(BSA_TMEM(oa, 16u, p.err), ov);
         }
       }
       tmem_wait_st();

@@ -70,6 +70,7 @@ bsa_status dkv_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
 bsa_status dq_launch(const bsa_bwd_args* a, const bsa_mask_info* info, float scale, cudaStream_t stream,
                      uint32_t* err = nullptr, bool schedule = true);
 bsa_status debug_wait_timeout_launch(cudaStream_t stream);
+bsa_status debug_selfcheck_launch(cudaStream_t stream);
 
 int num_sms();
 

@@ -20,7 +20,70 @@ enum DeviceError : uint32_t {
   DEV_ERR_TIMEOUT = 1u,      // a bounded wait ran out
   DEV_ERR_BOUNDS = 2u,       // an index read from MaskInfo was out of range
   DEV_ERR_TMEM = 4u,         // tensor-memory allocation returned an unusable address
+  DEV_ERR_DEBUG = 8u,        // (range-checked build) an index out of range or an mbarrier phase skipped;
+                             // bits 16-31 hold the source line of the first violation (0xFFFF: phase)
 };
+
+// The range-checked build (compiled with -DBSA_DEBUG=1, libbsa_debug.so)
+// checks tensor-memory addresses, the global rows the kernels compute from
+// the schedule and MaskInfo, and after every completed mbarrier wait that
+// the barrier has not already completed the next phase as well (a waiter
+// that fell a whole phase behind).  A violation records DEV_ERR_DEBUG and
+// its source line in the kernel's error word and the index is replaced by
+// an in-range one, so the access stays in bounds.  The release build
+// compiles every check away.
+#ifndef BSA_DEBUG
+#define BSA_DEBUG 0
+#endif
+
+__device__ __forceinline__ void debug_violation(uint32_t* err, uint32_t line) {
+  if (!err) return;
+  uint32_t old = *reinterpret_cast<volatile uint32_t*>(err);
+  while (!(old >> 16)) {
+    const uint32_t prev = atomicCAS(err, old, old | DEV_ERR_DEBUG | ((line & 0xFFFFu) << 16));
+    if (prev == old) return;
+    old = prev;
+  }
+  atomicOr(err, DEV_ERR_DEBUG);
+}
+
+template <class T>
+__device__ __forceinline__ T debug_range(T v, T lo, T hi, uint32_t* err, uint32_t line) {
+#if BSA_DEBUG
+  if (v < lo || v >= hi) {
+    debug_violation(err, line);
+    return lo;
+  }
+#else
+  (void)lo;
+  (void)hi;
+  (void)err;
+  (void)line;
+#endif
+  return v;
+}
+
+// A tensor-memory address whose access spans `ncols` columns: the column
+// field plus ncols within the 512 allocated columns, the lane field one of
+// the four 32-lane quarters.
+__device__ __forceinline__ uint32_t debug_tmem(uint32_t addr, uint32_t ncols, uint32_t* err, uint32_t line) {
+#if BSA_DEBUG
+  const bool col_ok = (addr & 0xFFFFu) + ncols <= 512u;
+  const bool lane_ok = (addr >> 16) <= 96u && ((addr >> 16) & 31u) == 0u;
+  if (!col_ok || !lane_ok) {
+    debug_violation(err, line);
+    return col_ok ? addr : (addr & 0xFFFF0000u);
+  }
+#else
+  (void)ncols;
+  (void)err;
+  (void)line;
+#endif
+  return addr;
+}
+
+#define BSA_RANGE(v, lo, hi, err) ::bsa::debug_range((v), (lo), (hi), (err), __LINE__)
+#define BSA_TMEM(addr, ncols, err) ::bsa::debug_tmem((addr), (ncols), (err), __LINE__)
 
 struct WaitCtl {
   uint32_t* err;             // global error word (may be null)
@@ -112,12 +175,29 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, 
   }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false when
 // the CTA is aborting or the time limit ran out (the error is recorded).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
-  return mbar_wait_slow(a, parity, w.err, w.abort, w.limit_ns);
+  const bool ok = mbar_try_wait(a, parity) || mbar_wait_slow(a, parity, w.err, w.abort, w.limit_ns);
+#if BSA_DEBUG
+  // every waiter of these barriers gates their next phase: right after the
+  // phase waited for, the next one cannot be complete yet
+  if (ok && mbar_test_wait(a, parity ^ 1u)) debug_violation(w.err, 0xFFFFu);
+#endif
+  return ok;
 }
 
 // The same wait by every lane of a warp, with a warp-uniform result (so that

@@ -306,7 +306,9 @@ BSA_API bsa_status bsa_bwd_noalloc(const bsa_bwd_args* args, const bsa_mask_info
 
 /* Synchronises `stream`, returns the device error word of the current
  * device in *word (0 = none; bit 1 = a bounded wait ran out, bit 2 =
- * out-of-range MaskInfo index, bit 4 = tensor-memory allocation failure)
+ * out-of-range MaskInfo index, bit 4 = tensor-memory allocation failure,
+ * bit 8 = a check of the range-checked build, whose source line is in
+ * bits 16-31)
  * and clears it.  The word is the OR of the library's word (set by every
  * launch but those of bsa_bwd_noalloc) and bsa_bwd_noalloc's own; a word
  * no launch has set up yet reads as 0, and nothing is allocated here.  The
@@ -321,6 +323,16 @@ BSA_API bsa_status bsa_set_wait_limit_ns(uint64_t ns);
  * the current wait limit, and returns.  Used to check that a wait that runs
  * out ends with BSA_ERR_TIMEOUT in the device error word instead of a hang. */
 BSA_API bsa_status bsa_debug_wait_timeout(bsa_stream stream);
+
+/* Launches one thread that passes out-of-range indices through the kernels'
+ * range checks.  In the range-checked build of the library (libbsa_debug.so,
+ * compiled with -DBSA_DEBUG=1: tensor-memory addresses, the global rows the
+ * kernels compute and the phases of mbarriers are checked on the device)
+ * the device error word then holds bit 8 (DEV_ERR_DEBUG) with the source
+ * line of the first violation in bits 16-31; in the release build the
+ * checks are compiled out and the word stays 0.  Used to check that the
+ * range-checked build reports what it finds. */
+BSA_API bsa_status bsa_debug_selfcheck(bsa_stream stream);
 
 BSA_API const char* bsa_status_string(bsa_status s);
 BSA_API const char* bsa_last_error(void);

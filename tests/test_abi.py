@@ -224,3 +224,15 @@ def test_noalloc_ignores_the_dsum_pointer_but_bwd_needs_it():
     # MaskInfo checks (null MaskInfo -> invalid argument, with that message)
     assert L.bsa_bwd_noalloc(C.byref(a), None, None, None) == _abi.INVALID_ARG
     assert b"MaskInfo" in L.bsa_last_error()
+
+
+def test_range_checked_library_exports_the_same_symbols():
+    """The range-checked variant (built by build(), loaded when
+    BSA_LIBRARY_VARIANT=debug) exports every symbol the header declares."""
+    import ctypes
+    from block_sparse_attention_process_gb300 import build as b
+    if not os.path.exists(b.LIB_DEBUG):
+        pytest.skip("range-checked library not built")
+    L = ctypes.CDLL(b.LIB_DEBUG)
+    for n in declared_symbols():
+        assert hasattr(L, n), n
