@@ -47,6 +47,7 @@ namespace {
 constexpr int kStagesK = 2;
 constexpr int kStagesV = 2;
 constexpr int kSBufs = 2;         // score buffers in TMEM
+static_assert(kStagesK == kSBufs && kStagesV == kSBufs, "K stage, V stage and score buffer of a block share its index");
 constexpr int kInfoRing = 32;     // block descriptors published by the walker warp
 // The softmax is split over kParts warpgroups, each taking kCols of the 128
 // score columns of every row (and D / kParts of the O columns).
@@ -81,9 +82,12 @@ struct __align__(1024) FwdSmem {
   // (128-byte swizzle, the layout of the output tensor map's box)
   uint8_t ostage[4][32 * 128];
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStagesK], k_empty[kStagesK];
+  uint64_t k_full[kStagesK];
   uint64_t v_full[kStagesV], v_empty[kStagesV];
-  uint64_t s_full[kSBufs], p_full[kSBufs], pv_done[kSBufs];
+  // s_full[b] also frees K stage b (the scores of a block are the only
+  // reader of its K) and v_empty[b] marks block n's P V done for the
+  // softmax's rescale (b = n mod 2 for both)
+  uint64_t s_full[kSBufs], p_full[kSBufs];
   uint64_t o_full, o_empty, drain;
   uint64_t info_full[kInfoRing], info_empty[kInfoRing];
   // per block: {col | label<<16 | flags, stack slot, q_sequence of the tile's first query,
@@ -158,11 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 32 * kSoftmaxWarps);
-      mbar_init(&s.pv_done[i], 1);
     }
     for (int i = 0; i < kStagesK; ++i) {
       mbar_init(&s.k_full[i], 1);
-      mbar_init(&s.k_empty[i], 1);
     }
     for (int i = 0; i < kStagesV; ++i) {
       mbar_init(&s.v_full[i], 1);
@@ -315,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qrow = s.binfo[slot].w;
         const uint32_t krow = s.bkrow[slot];
         const uint32_t ks = k_loads % kStagesK;
-        if (k_loads >= kStagesK && !mbar_wait(&s.k_empty[ks], ((k_loads / kStagesK) - 1) & 1u, wc)) { ok = false; break; }
+        // stage ks is free once the scores of the block two back are ready
+        if (k_loads >= kStagesK && !mbar_wait(&s.s_full[ks], ((k_loads / kStagesK) - 1) & 1u, wc)) { ok = false; break; }
         if (x & kEnd) {
           // no more blocks: complete the stage without data so the MMA warp reads the end mark
           mbar_arrive(&s.k_full[ks]);
@@ -411,8 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
         mma_ss_elect(BSA_TMEM(tmem + sb * 128, 128u, p.err), cur_q + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
-      mma_commit_elect(&s.s_full[sb]);
-      mma_commit_elect(&s.k_empty[ks]);
+      mma_commit_elect(&s.s_full[sb]);  // also frees K stage ks (== sb)
       if (info & kLast) {  // last block of the tile: its Q buffer is free after this S
         mma_commit_elect(&s.q_empty[q_uses & 1u]);
         ++q_uses;
@@ -429,10 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t fl = (flags >> (2u * (pv_cnt & 7u))) & 3u;
       const bool pv_first = fl & 1u, pv_last = fl & 2u;
       const uint32_t pb = pv_cnt % kSBufs;
-      if (!mbar_wait_warp(&s.p_full[pb], (pv_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
-      if (pv_first && o_uses > 0 && !mbar_wait_warp(&s.o_empty, (o_uses - 1) & 1u, wc)) { ok = false; break; }
+      // V and the accumulator (usually long ready) first: the wait for P is
+      // the one the tensor pipe idles on, and P V follows it directly
       const uint32_t vs = pv_cnt % kStagesV;
       if (!mbar_wait_warp(&s.v_full[vs], (pv_cnt / kStagesV) & 1u, wc)) { ok = false; break; }
+      if (pv_first && o_uses > 0 && !mbar_wait_warp(&s.o_empty, (o_uses - 1) & 1u, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(&s.p_full[pb], (pv_cnt / kSBufs) & 1u, wc)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = vdesc0 + vs * kTileDesc;
       // part p's P (keys [64p, 64p + 64), words [64p, 64p + 32) of the
@@ -441,8 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < 8; ++kk)
         mma_ts_elect(BSA_TMEM(tmem + kTmemO + (kk >> 2) * 128, 128u, p.err), BSA_TMEM(tmem + pb * 128 + (kk >> 2) * 64 + (kk & 3) * 8, 8u, p.err),
                      vd + static_cast<uint64_t>(kk * 2048 >> 4), idesc_o, (pv_first && (kk & 3) == 0) ? 0u : 1u);
-      mma_commit_elect(&s.v_empty[vs]);
-      mma_commit_elect(&s.pv_done[pb]);
+      mma_commit_elect(&s.v_empty[vs]);  // also: this P V done (vs == pb)
       if (pv_last) {
         mma_commit_elect(&s.o_full);
         ++o_uses;
@@ -593,10 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++tiles;
       return true;
     };
+    // block descriptors from the walker (published long before their
+    // scores); the next one's barrier is tested while a block is computed
+    if (!mbar_wait_warp(&s.info_full[0], 0u, wc)) ok = false;
     while (ok) {
-      // block descriptor from the walker (published long before its scores)
       const uint32_t slot = n % kInfoRing;
-      if (!mbar_wait_warp(&s.info_full[slot], (n / kInfoRing) & 1u, wc)) { ok = false; break; }
       const uint4 bi = s.binfo[slot];
       if (bi.x & kEnd) break;
       const uint32_t sb = n % kSBufs;
@@ -665,6 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kCols; c += 32) tmem_ld32(BSA_TMEM(tmem + sb * 128 + col0 + c + lane_off, 32u, p.err), xu + c);
       tmem_wait_ld();
       reg_fence<kCols>(xu);
+      const uint32_t nslot = (n + 1) % kInfoRing;
+      const bool next_ready = mbar_test_wait(smem_u32(&s.info_full[nslot]), ((n + 1) / kInfoRing) & 1u);
       if (label == 1) {
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
@@ -742,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // part's accumulator (after the previous P V has landed) when its max moved.
       if (warp_switch && exec > 0) {
         const uint32_t prev = n - 1;
-        if (!mbar_wait_warp(&s.pv_done[prev % kSBufs], (prev / kSBufs) & 1u, wc)) { ok = false; break; }
+        if (!mbar_wait_warp(&s.v_empty[prev % kStagesV], (prev / kStagesV) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
         const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
@@ -769,6 +775,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n;
       ++exec;
       if (last && !finish_tile(bi.w)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, next_ready) && !mbar_wait_warp(&s.info_full[nslot], (n / kInfoRing) & 1u, wc)) {
+        ok = false;
+        break;
+      }
     }
     // end mark for the epilogue warpgroup
     if (ok) {
