@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
 // ===========================================================================
 // dK / dV launch
 // ===========================================================================
-constexpr int kDkvStages = 2;        // (Q, dO, LSE, Dsum) of one query block
+constexpr int kDkvStages = 2;        // (Q, LSE, Dsum) and dO of one query block
 constexpr uint32_t kDkvColST = 0;    // S^T, then P^T (bf16) over it
 constexpr uint32_t kDkvColDP = 128;  // dP^T, then dS^T (bf16) over it
 constexpr uint32_t kDkvColDV = 256;
@@ -717,10 +717,15 @@ struct __align__(1024) DkvSmem {
   float lse[kDkvStages][128];
   float dsum[kDkvStages][128];
   uint64_t k_full, k_empty, v_full, v_empty;
-  // in_empty: the MMA warp's commit after an item's dK, plus one arrival per
-  // elementwise warp (at a tile's last item, once its tensor stores out of
-  // the item's Q / dO buffers have read them; otherwise from the MMA warp)
-  uint64_t in_full[kDkvStages], in_empty[kDkvStages];
+  // An item's inputs in two stages of their own: Q (with LSE and Dsum), read
+  // up to its dK, and dO, read up to its dV (one GEMM earlier), so that the
+  // next dO loads while the current item's last MMAs run and Q, which the
+  // next item needs first, loads alone.  q_empty / do_empty: the MMA warp's
+  // commit after the item's dK / dV, plus one arrival per elementwise warp
+  // (at a tile's last item, once its tensor stores out of the item's Q / dO
+  // buffers have read them; otherwise from the MMA warp).
+  uint64_t q_full[kDkvStages], q_empty[kDkvStages];
+  uint64_t do_full[kDkvStages], do_empty[kDkvStages];
   // p_full[h]: half h of every thread's query columns of P^T is in tensor
   // memory (dV takes those k-steps first)
   uint64_t st_full, dpt_full, p_full[2], ds_full;
@@ -867,8 +872,10 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     mbar_init(&s.v_full, 1);
     mbar_init(&s.v_empty, 1);
     for (int i = 0; i < kDkvStages; ++i) {
-      mbar_init(&s.in_full[i], 1);
-      mbar_init(&s.in_empty[i], 1 + 4 * DkvShape<D>::kParts);
+      mbar_init(&s.q_full[i], 1);
+      mbar_init(&s.q_empty[i], 1 + 4 * DkvShape<D>::kParts);
+      mbar_init(&s.do_full[i], 1);
+      mbar_init(&s.do_empty[i], 1 + 4 * DkvShape<D>::kParts);
     }
     mbar_init(&s.st_full, 1);
     mbar_init(&s.dpt_full, 1);
@@ -903,7 +910,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       tma_prefetch_desc(&tm_do);
       const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      uint32_t k_loads = 0, v_loads = 0, in_loads = 0;
+      uint32_t k_loads = 0, v_loads = 0, in_loads = 0, do_loads = 0;
       bool ok = true;
       DkvTile t;
       for (int32_t kt = 0; ok && dkv_tile(p, kt, t); ++kt) {
@@ -916,20 +923,24 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         for (int32_t x = 0; x < t.total && ok; ++x) {
           it.next(p, t, hq, br);
           const uint32_t st = in_loads % kDkvStages;
-          if (in_loads >= kDkvStages && !mbar_wait(&s.in_empty[st], ((in_loads / kDkvStages) - 1) & 1u, wc)) { ok = false; break; }
+          const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + hq) * p.Sq + br.col * 128;
+          // dO first: its stage frees one GEMM before Q's
+          if (in_loads >= kDkvStages && !mbar_wait(&s.do_empty[st], ((in_loads / kDkvStages) - 1) & 1u, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.do_full[st], kTile);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(s.dout[st] + c * 16384, &tm_do, &s.do_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
+          ++do_loads;
+          if (in_loads >= kDkvStages && !mbar_wait(&s.q_empty[st], ((in_loads / kDkvStages) - 1) & 1u, wc)) { ok = false; break; }
           const uint32_t extra = p.mi.kind == BSA_MASK_DENSE ? static_cast<uint32_t>(br.slot)
                                                              : static_cast<uint32_t>(p.mi.q_sequence[br.col * 128]);
           s.binfo[in_loads % kInfoRing] = make_uint4(pack_info(br.col, br.label, x == 0, x == t.total - 1), extra,
                                                      static_cast<uint32_t>(t.j * 128),
                                                      static_cast<uint32_t>(dkv_out_row(p, t, krow)));
-          mbar_arrive_expect_tx(&s.in_full[st], 2 * kTile + 1024);
-          const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + hq) * p.Sq + br.col * 128;
-          for (int c = 0; c < kChunks; ++c) {
-            tma_load_2d(s.q[st] + c * 16384, &tm_q, &s.in_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
-            tma_load_2d(s.dout[st] + c * 16384, &tm_do, &s.in_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
-          }
-          bulk_load(s.lse[st], p.lse + qrow, 512, &s.in_full[st]);
-          bulk_load(s.dsum[st], p.dsum + qrow, 512, &s.in_full[st]);
+          mbar_arrive_expect_tx(&s.q_full[st], kTile + 1024);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(s.q[st] + c * 16384, &tm_q, &s.q_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
+          bulk_load(s.lse[st], p.lse + qrow, 512, &s.q_full[st]);
+          bulk_load(s.dsum[st], p.dsum + qrow, 512, &s.q_full[st]);
           ++in_loads;
           if (x > 0) continue;
           // The tile's K and V follow its first query block, so that this
@@ -961,7 +972,9 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         if (k_loads) (void)mbar_wait(&s.k_full, (k_loads - 1) & 1u, dw);
         if (v_loads) (void)mbar_wait(&s.v_full, (v_loads - 1) & 1u, dw);
         for (uint32_t i = (in_loads > kDkvStages ? in_loads - kDkvStages : 0); i < in_loads; ++i)
-          (void)mbar_wait(&s.in_full[i % kDkvStages], (i / kDkvStages) & 1u, dw);
+          (void)mbar_wait(&s.q_full[i % kDkvStages], (i / kDkvStages) & 1u, dw);
+        for (uint32_t i = (do_loads > kDkvStages ? do_loads - kDkvStages : 0); i < do_loads; ++i)
+          (void)mbar_wait(&s.do_full[i % kDkvStages], (i / kDkvStages) & 1u, dw);
       }
     }
   } else if (warp == 1) {
@@ -993,7 +1006,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     uint32_t flags = 0;  // first/last bits of items n and n+1, two per item
     auto item_flags = [&](uint32_t k) -> bool {
       const uint32_t st = k % kDkvStages;
-      if (!mbar_wait_warp(&s.in_full[st], (k / kDkvStages) & 1u, wc)) return false;
+      if (!mbar_wait_warp(&s.q_full[st], (k / kDkvStages) & 1u, wc)) return false;
       const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[k % kInfoRing].x, 0);
       const uint32_t sh = 2u * (k & 7u);
       flags = (flags & ~(3u << sh)) | (((info >> 20) & 3u) << sh);
@@ -1019,8 +1032,9 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       if ((flags >> (2u * (k & 7u))) & 1u) {  // first item of a tile: its V
         if (!mbar_wait_warp(&s.v_full, v_uses & 1u, wc)) return false;
         ++v_uses;
-        tc_fence_after();
       }
+      if (!mbar_wait_warp(&s.do_full[k % kDkvStages], (k / kDkvStages) & 1u, wc)) return false;
+      tc_fence_after();
       const uint64_t dod = dodesc0 + (k % kDkvStages) * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -1069,6 +1083,10 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         }
         if (!half_ok) { ok = false; break; }
       }
+      // dO is read by dP^T and dV only; the elementwise warps' share of
+      // do_empty comes from here except at a tile's last item
+      mma_commit_elect(&s.do_empty[st]);
+      if (!last) mbar_arrive_cnt_elect(&s.do_empty[st], 4 * DkvShape<D>::kParts);
       // next item's S^T over the P^T columns the dV MMA has just read
       if (more && !last) {
         if (!item_flags(n + 1)) { ok = false; break; }
@@ -1083,16 +1101,16 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         mma_ts_elect(BSA_TMEM(tmem + kDkvColDK, 128u, p.err), BSA_TMEM(tmem + kDkvColDP + part_a_col<DkvShape<D>::kCols>(kk), 8u, p.err),
                      qmn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
-      mma_commit_elect(&s.in_empty[st]);
+      mma_commit_elect(&s.q_empty[st]);
       if (last) {
         mma_commit_elect(&s.acc_full);
         ++acc_uses;
-      } else if (lane == 0) {
-        // the elementwise warps' share of in_empty (they only hold the Q / dO
-        // buffers of a tile's last item, for the epilogue's tensor stores)
-        mbar_arrive_cnt(&s.in_empty[st], 4 * DkvShape<D>::kParts);
+      } else {
+        // the elementwise warps' share of q_empty (they only hold the Q / dO
+        // buffers of a tile's last item, for the epilogue's tensor stores;
+        // their reads of LSE and Dsum end before dK)
+        mbar_arrive_cnt_elect(&s.q_empty[st], 4 * DkvShape<D>::kParts);
       }
-      __syncwarp();
       if (more) {
         if (last) {
           if (!item_flags(n + 1)) { ok = false; break; }
@@ -1135,7 +1153,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     const uint64_t nsc2 = f2_pack(-p.scale, -p.scale), nl2e2 = f2_pack(-kLog2e, -kLog2e);
     for (uint32_t n = 0; ok && n < total; ++n) {
       const uint32_t st = n % kDkvStages;
-      if (!mbar_wait_warp(&s.in_full[st], (n / kDkvStages) & 1u, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(&s.q_full[st], (n / kDkvStages) & 1u, wc)) { ok = false; break; }
       const uint4 bi = s.binfo[n % kInfoRing];
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
@@ -1265,7 +1283,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       if (!sp && !p.grad_fp32) {
         // bf16 dV and dK through shared memory: the last item's dO and Q
         // buffers are free (its MMAs have completed) and stay the
-        // elementwise warps' until each releases them on in_empty.  A warp's
+        // elementwise warps' until each releases them on q_empty and do_empty.  A warp's
         // [32 keys, 32 columns] of each goes out in one tensor store.
         uint8_t* stv = s.dout[st] + (warp - 4) * 2048;
         uint8_t* stk = s.q[st] + (warp - 4) * 2048;
@@ -1288,7 +1306,8 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           tma_store_2d(&tm_dk, stk, part * kPartD, row0);
           tma_store_commit();
           tma_store_wait_read();
-          mbar_arrive(&s.in_empty[st]);
+          mbar_arrive(&s.q_empty[st]);
+          mbar_arrive(&s.do_empty[st]);
         }
         __syncwarp();
       } else {
@@ -1303,7 +1322,10 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         store_row(sp ? p.part_dk : p.dk, sp ? 1 : p.grad_fp32, krow, D, v, part * kPartD, p.scale);
         tc_fence_before();
         mbar_arrive(&s.acc_empty);
-        if (lane == 0) mbar_arrive(&s.in_empty[st]);
+        if (lane == 0) {
+          mbar_arrive(&s.q_empty[st]);
+          mbar_arrive(&s.do_empty[st]);
+        }
       }
       ++acc_uses;
     }
