@@ -701,7 +701,9 @@ __global__ void __launch_bounds__(DqShape<D>::kThreads, 1)
 // ===========================================================================
 // dK / dV launch
 // ===========================================================================
-constexpr int kDkvStages = 2;        // (Q, LSE, Dsum) and dO of one query block
+constexpr int kDkvQStages = 3;       // Q of one query block
+constexpr int kDkvDoStages = 2;      // (dO, LSE, Dsum) of one query block
+constexpr int kDkvInfoRing = 8;      // item descriptors (written with an item's Q)
 constexpr uint32_t kDkvColST = 0;    // S^T, then P^T (bf16) over it
 constexpr uint32_t kDkvColDP = 128;  // dP^T, then dS^T (bf16) over it
 constexpr uint32_t kDkvColDV = 256;
@@ -712,30 +714,37 @@ struct __align__(1024) DkvSmem {
   static constexpr int kTile = 128 * D * 2;
   uint8_t k[kTile];
   uint8_t v[kTile];
-  uint8_t q[kDkvStages][kTile];
-  uint8_t dout[kDkvStages][kTile];
-  float lse[kDkvStages][128];
-  float dsum[kDkvStages][128];
+  uint8_t q[kDkvQStages][kTile];
+  uint8_t dout[kDkvDoStages][kTile];
+  float lse[kDkvDoStages][128];
+  float dsum[kDkvDoStages][128];
   uint64_t k_full, k_empty, v_full, v_empty;
-  // An item's inputs in two stages of their own: Q (with LSE and Dsum), read
-  // up to its dK, and dO, read up to its dV (one GEMM earlier), so that the
-  // next dO loads while the current item's last MMAs run and Q, which the
-  // next item needs first, loads alone.  q_empty / do_empty: the MMA warp's
-  // commit after the item's dK / dV, plus one arrival per elementwise warp
-  // (at a tile's last item, once its tensor stores out of the item's Q / dO
-  // buffers have read them; otherwise from the MMA warp).
-  uint64_t q_full[kDkvStages], q_empty[kDkvStages];
-  uint64_t do_full[kDkvStages], do_empty[kDkvStages];
+  // An item's inputs in stages of their own: Q, read up to the item's dK
+  // and needed first by the next items (three stages, so that a load has
+  // two items' time to land), and (dO, LSE, Dsum), read up to the item's dV
+  // and dS (two stages).  q_empty: the MMA warp's commit after the item's
+  // dK plus one arrival per elementwise warp (from the MMA warp, except at a
+  // tile's last item, where the elementwise warps arrive once their tensor
+  // stores out of the item's Q buffer have read it); do_empty: the commit
+  // after the item's dV plus one arrival per elementwise warp once it has
+  // computed dS (or, at a tile's last item, once its stores out of the dO
+  // buffer have read it).
+  uint64_t q_full[kDkvQStages], q_empty[kDkvQStages];
+  uint64_t do_full[kDkvDoStages], do_empty[kDkvDoStages];
   // p_full[h]: half h of every thread's query columns of P^T is in tensor
   // memory (dV takes those k-steps first)
   uint64_t st_full, dpt_full, p_full[2], ds_full;
   uint64_t acc_full, acc_empty, drain;
   // per item: {col | label<<16 | first<<20 | last<<21, stack slot (dense) or q_sequence of the
   // query block's first row (computable), 128*j = first key of the tile, row of that key in dK/dV}
-  uint4 binfo[kInfoRing];
+  uint4 binfo[kDkvInfoRing];
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+// The layout starts on a 1024-byte boundary (128-byte swizzled tiles); the
+// dynamic shared memory of a launch does (the kernel checks it), so no slack
+// is requested and the three Q stages fit.
+static_assert(sizeof(DkvSmem<128>) <= 232448, "dK/dV shared memory exceeds 227 KB per CTA");
 
 struct DkvTile {
   int32_t b, g, j;
@@ -859,11 +868,15 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
                const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   using Smem = DkvSmem<D>;
-  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw);
   constexpr uint32_t kTile = Smem::kTile;
   constexpr int kChunks = D / 64;
   const int warp = warp_id();
   const int lane = threadIdx.x & 31;
+  if (smem_u32(smem_raw) & 1023u) {  // (uniform over the CTA) nothing has been touched yet
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_SMEM_ALIGN);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -871,9 +884,11 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     mbar_init(&s.k_empty, 1);
     mbar_init(&s.v_full, 1);
     mbar_init(&s.v_empty, 1);
-    for (int i = 0; i < kDkvStages; ++i) {
+    for (int i = 0; i < kDkvQStages; ++i) {
       mbar_init(&s.q_full[i], 1);
       mbar_init(&s.q_empty[i], 1 + 4 * DkvShape<D>::kParts);
+    }
+    for (int i = 0; i < kDkvDoStages; ++i) {
       mbar_init(&s.do_full[i], 1);
       mbar_init(&s.do_empty[i], 1 + 4 * DkvShape<D>::kParts);
     }
@@ -922,26 +937,27 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         BlockRef br;
         for (int32_t x = 0; x < t.total && ok; ++x) {
           it.next(p, t, hq, br);
-          const uint32_t st = in_loads % kDkvStages;
           const int64_t qrow = (static_cast<int64_t>(t.b) * p.Hq + hq) * p.Sq + br.col * 128;
-          // dO first: its stage frees one GEMM before Q's
-          if (in_loads >= kDkvStages && !mbar_wait(&s.do_empty[st], ((in_loads / kDkvStages) - 1) & 1u, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.do_full[st], kTile);
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(s.dout[st] + c * 16384, &tm_do, &s.do_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
-          ++do_loads;
-          if (in_loads >= kDkvStages && !mbar_wait(&s.q_empty[st], ((in_loads / kDkvStages) - 1) & 1u, wc)) { ok = false; break; }
+          // Q (needed first, by the item's S^T), then dO with LSE and Dsum
+          const uint32_t qs = in_loads % kDkvQStages;
+          if (in_loads >= kDkvQStages && !mbar_wait(&s.q_empty[qs], ((in_loads / kDkvQStages) - 1) & 1u, wc)) { ok = false; break; }
           const uint32_t extra = p.mi.kind == BSA_MASK_DENSE ? static_cast<uint32_t>(br.slot)
                                                              : static_cast<uint32_t>(p.mi.q_sequence[br.col * 128]);
-          s.binfo[in_loads % kInfoRing] = make_uint4(pack_info(br.col, br.label, x == 0, x == t.total - 1), extra,
+          s.binfo[in_loads % kDkvInfoRing] = make_uint4(pack_info(br.col, br.label, x == 0, x == t.total - 1), extra,
                                                      static_cast<uint32_t>(t.j * 128),
                                                      static_cast<uint32_t>(dkv_out_row(p, t, krow)));
-          mbar_arrive_expect_tx(&s.q_full[st], kTile + 1024);
+          mbar_arrive_expect_tx(&s.q_full[qs], kTile);
           for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(s.q[st] + c * 16384, &tm_q, &s.q_full[st], c * 64, static_cast<int32_t>(qrow), pol_q);
-          bulk_load(s.lse[st], p.lse + qrow, 512, &s.q_full[st]);
-          bulk_load(s.dsum[st], p.dsum + qrow, 512, &s.q_full[st]);
+            tma_load_2d(s.q[qs] + c * 16384, &tm_q, &s.q_full[qs], c * 64, static_cast<int32_t>(qrow), pol_q);
           ++in_loads;
+          const uint32_t ds = do_loads % kDkvDoStages;
+          if (do_loads >= kDkvDoStages && !mbar_wait(&s.do_empty[ds], ((do_loads / kDkvDoStages) - 1) & 1u, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.do_full[ds], kTile + 1024);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(s.dout[ds] + c * 16384, &tm_do, &s.do_full[ds], c * 64, static_cast<int32_t>(qrow), pol_q);
+          bulk_load(s.lse[ds], p.lse + qrow, 512, &s.do_full[ds]);
+          bulk_load(s.dsum[ds], p.dsum + qrow, 512, &s.do_full[ds]);
+          ++do_loads;
           if (x > 0) continue;
           // The tile's K and V follow its first query block, so that this
           // block's loads do not wait for the previous tile's last MMAs: K is
@@ -971,10 +987,10 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         WaitCtl dw{nullptr, &dummy_abort, p.wait_ns};
         if (k_loads) (void)mbar_wait(&s.k_full, (k_loads - 1) & 1u, dw);
         if (v_loads) (void)mbar_wait(&s.v_full, (v_loads - 1) & 1u, dw);
-        for (uint32_t i = (in_loads > kDkvStages ? in_loads - kDkvStages : 0); i < in_loads; ++i)
-          (void)mbar_wait(&s.q_full[i % kDkvStages], (i / kDkvStages) & 1u, dw);
-        for (uint32_t i = (do_loads > kDkvStages ? do_loads - kDkvStages : 0); i < do_loads; ++i)
-          (void)mbar_wait(&s.do_full[i % kDkvStages], (i / kDkvStages) & 1u, dw);
+        for (uint32_t i = (in_loads > kDkvQStages ? in_loads - kDkvQStages : 0); i < in_loads; ++i)
+          (void)mbar_wait(&s.q_full[i % kDkvQStages], (i / kDkvQStages) & 1u, dw);
+        for (uint32_t i = (do_loads > kDkvDoStages ? do_loads - kDkvDoStages : 0); i < do_loads; ++i)
+          (void)mbar_wait(&s.do_full[i % kDkvDoStages], (i / kDkvDoStages) & 1u, dw);
       }
     }
   } else if (warp == 1) {
@@ -1005,9 +1021,8 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     // loads.
     uint32_t flags = 0;  // first/last bits of items n and n+1, two per item
     auto item_flags = [&](uint32_t k) -> bool {
-      const uint32_t st = k % kDkvStages;
-      if (!mbar_wait_warp(&s.q_full[st], (k / kDkvStages) & 1u, wc)) return false;
-      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[k % kInfoRing].x, 0);
+      if (!mbar_wait_warp(&s.q_full[k % kDkvQStages], (k / kDkvQStages) & 1u, wc)) return false;
+      const uint32_t info = __shfl_sync(0xffffffffu, s.binfo[k % kDkvInfoRing].x, 0);
       const uint32_t sh = 2u * (k & 7u);
       flags = (flags & ~(3u << sh)) | (((info >> 20) & 3u) << sh);
       if ((info >> 20) & 1u) {  // first item of a tile: its K
@@ -1018,7 +1033,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       return true;
     };
     auto issue_st = [&](uint32_t k) {
-      const uint64_t qd = qdesc0 + (k % kDkvStages) * kTileDesc;
+      const uint64_t qd = qdesc0 + (k % kDkvQStages) * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -1033,9 +1048,9 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         if (!mbar_wait_warp(&s.v_full, v_uses & 1u, wc)) return false;
         ++v_uses;
       }
-      if (!mbar_wait_warp(&s.do_full[k % kDkvStages], (k / kDkvStages) & 1u, wc)) return false;
+      if (!mbar_wait_warp(&s.do_full[k % kDkvDoStages], (k / kDkvDoStages) & 1u, wc)) return false;
       tc_fence_after();
-      const uint64_t dod = dodesc0 + (k % kDkvStages) * kTileDesc;
+      const uint64_t dod = dodesc0 + (k % kDkvDoStages) * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -1054,7 +1069,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       }
     }
     for (uint32_t n = 0; ok && n < total; ++n) {
-      const uint32_t st = n % kDkvStages;
+      const uint32_t qs = n % kDkvQStages, ds = n % kDkvDoStages;
       const uint32_t fl = (flags >> (2u * (n & 7u))) & 3u;
       const bool first = fl & 1u, last = fl & 2u;
       const bool more = n + 1 < total;
@@ -1063,7 +1078,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       if (!mbar_wait_warp(&s.p_full[0], n & 1u, wc)) { ok = false; break; }
       if (first && acc_uses > 0 && !mbar_wait_warp(&s.acc_empty, (acc_uses - 1) & 1u, wc)) { ok = false; break; }
       tc_fence_after();
-      const uint64_t domn = domn0 + st * kTileDesc;
+      const uint64_t domn = domn0 + ds * kTileDesc;
       {
         constexpr int kSteps = DkvShape<D>::kCols / 16;  // k-steps per part
         bool half_ok = true;
@@ -1083,10 +1098,9 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         }
         if (!half_ok) { ok = false; break; }
       }
-      // dO is read by dP^T and dV only; the elementwise warps' share of
-      // do_empty comes from here except at a tile's last item
-      mma_commit_elect(&s.do_empty[st]);
-      if (!last) mbar_arrive_cnt_elect(&s.do_empty[st], 4 * DkvShape<D>::kParts);
+      // dO is read by dP^T and dV only (the elementwise warps add their
+      // arrivals once dS is computed)
+      mma_commit_elect(&s.do_empty[ds]);
       // next item's S^T over the P^T columns the dV MMA has just read
       if (more && !last) {
         if (!item_flags(n + 1)) { ok = false; break; }
@@ -1095,21 +1109,20 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       // dK += dS^T Q
       if (!mbar_wait_warp(&s.ds_full, n & 1u, wc)) { ok = false; break; }
       tc_fence_after();
-      const uint64_t qmn = qmn0 + st * kTileDesc;
+      const uint64_t qmn = qmn0 + qs * kTileDesc;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ts_elect(BSA_TMEM(tmem + kDkvColDK, 128u, p.err), BSA_TMEM(tmem + kDkvColDP + part_a_col<DkvShape<D>::kCols>(kk), 8u, p.err),
                      qmn + static_cast<uint64_t>(kk * 2048 >> 4),
                      idesc_acc, (first && kk == 0) ? 0u : 1u);
-      mma_commit_elect(&s.q_empty[st]);
+      mma_commit_elect(&s.q_empty[qs]);
       if (last) {
         mma_commit_elect(&s.acc_full);
         ++acc_uses;
       } else {
-        // the elementwise warps' share of q_empty (they only hold the Q / dO
-        // buffers of a tile's last item, for the epilogue's tensor stores;
-        // their reads of LSE and Dsum end before dK)
-        mbar_arrive_cnt_elect(&s.q_empty[st], 4 * DkvShape<D>::kParts);
+        // the elementwise warps' share of q_empty (they hold the Q buffer
+        // only at a tile's last item, for the epilogue's tensor stores)
+        mbar_arrive_cnt_elect(&s.q_empty[qs], 4 * DkvShape<D>::kParts);
       }
       if (more) {
         if (last) {
@@ -1152,9 +1165,9 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
     int64_t lo = 0, hi = 0, krow = 0;
     const uint64_t nsc2 = f2_pack(-p.scale, -p.scale), nl2e2 = f2_pack(-kLog2e, -kLog2e);
     for (uint32_t n = 0; ok && n < total; ++n) {
-      const uint32_t st = n % kDkvStages;
-      if (!mbar_wait_warp(&s.q_full[st], (n / kDkvStages) & 1u, wc)) { ok = false; break; }
-      const uint4 bi = s.binfo[n % kInfoRing];
+      const uint32_t st = n % kDkvDoStages;  // LSE and Dsum of this item
+      if (!mbar_wait_warp(&s.do_full[st], (n / kDkvDoStages) & 1u, wc)) { ok = false; break; }
+      const uint4 bi = s.binfo[n % kDkvInfoRing];
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = (bi.x >> 20) & 1u, last = (bi.x >> 21) & 1u;
       if (first) {
@@ -1275,7 +1288,11 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.ds_full);
-      if (!last) continue;
+      if (!last) {
+        // done with this item's LSE and Dsum
+        if (lane == 0) mbar_arrive(&s.do_empty[st]);
+        continue;
+      }
       if (!mbar_wait_warp(&s.acc_full, acc_uses & 1u, wc)) { ok = false; break; }
       tc_fence_after();
       static_assert(kPartD == 32, "one 32-column slice of dK and dV per thread");
@@ -1286,7 +1303,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         // elementwise warps' until each releases them on q_empty and do_empty.  A warp's
         // [32 keys, 32 columns] of each goes out in one tensor store.
         uint8_t* stv = s.dout[st] + (warp - 4) * 2048;
-        uint8_t* stk = s.q[st] + (warp - 4) * 2048;
+        uint8_t* stk = s.q[n % kDkvQStages] + (warp - 4) * 2048;
         uint32_t v[32];
         tmem_ld32(BSA_TMEM(tmem + kDkvColDV + part * kPartD + lane_off, 32u, p.err), v);
         tmem_wait_ld();
@@ -1306,7 +1323,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           tma_store_2d(&tm_dk, stk, part * kPartD, row0);
           tma_store_commit();
           tma_store_wait_read();
-          mbar_arrive(&s.q_empty[st]);
+          mbar_arrive(&s.q_empty[n % kDkvQStages]);
           mbar_arrive(&s.do_empty[st]);
         }
         __syncwarp();
@@ -1323,7 +1340,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(&s.acc_empty);
         if (lane == 0) {
-          mbar_arrive(&s.q_empty[st]);
+          mbar_arrive(&s.q_empty[n % kDkvQStages]);
           mbar_arrive(&s.do_empty[st]);
         }
       }
@@ -1420,7 +1437,7 @@ bsa_status launch_dkv(const bsa_bwd_args* a, const bsa_mask_info* info, float sc
   const int variant = cap ? 2 : (info->kind == BSA_MASK_DENSE ? 1 : 0);
   auto kern = variant == 2 ? dkv_kernel<D, true, kAnyMask>
                            : (variant == 1 ? dkv_kernel<D, false, kDenseMask> : dkv_kernel<D, false, kComputableMask>);
-  const size_t smem = sizeof(DkvSmem<D>) + 1024;
+  const size_t smem = sizeof(DkvSmem<D>);  // no alignment slack: see DkvSmem
   {
     bsa_status st = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem, "set dkv smem size");
     if (st != BSA_OK) return st;

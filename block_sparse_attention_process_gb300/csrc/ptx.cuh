@@ -22,6 +22,7 @@ enum DeviceError : uint32_t {
   DEV_ERR_TMEM = 4u,         // tensor-memory allocation returned an unusable address
   DEV_ERR_DEBUG = 8u,        // (range-checked build) an index out of range or an mbarrier phase skipped;
                              // bits 16-31 hold the source line of the first violation (0xFFFF: phase)
+  DEV_ERR_SMEM_ALIGN = 16u,  // dynamic shared memory did not start on a 1024-byte boundary (the kernel did nothing)
 };
 
 // The range-checked build (compiled with -DBSA_DEBUG=1, libbsa_debug.so)

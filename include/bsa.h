@@ -305,14 +305,16 @@ BSA_API bsa_status bsa_bwd_noalloc(const bsa_bwd_args* args, const bsa_mask_info
                                    const bsa_mask_info* dkv_info, bsa_stream stream);
 
 /* Synchronises `stream`, returns the device error word of the current
- * device in *word (0 = none; bit 1 = a bounded wait ran out, bit 2 =
- * out-of-range MaskInfo index, bit 4 = tensor-memory allocation failure,
- * bit 8 = a check of the range-checked build, whose source line is in
- * bits 16-31)
- * and clears it.  The word is the OR of the library's word (set by every
- * launch but those of bsa_bwd_noalloc) and bsa_bwd_noalloc's own; a word
- * no launch has set up yet reads as 0, and nothing is allocated here.  The
- * status is BSA_ERR_TIMEOUT / BSA_ERR_DEVICE when the word is non-zero. */
+ * device in *word and clears it.  0 = none; otherwise an OR of the flags
+ * 1 = a bounded wait ran out, 2 = out-of-range MaskInfo index, 4 =
+ * tensor-memory allocation failure, 8 = a check of the range-checked build
+ * (the source line of the first one is then in bits 16-31 of the word),
+ * 16 = a kernel found its dynamic shared memory off the 1024-byte boundary
+ * it is laid out for, and did nothing.  The word is the OR of the
+ * library's word (set by every launch but those of bsa_bwd_noalloc) and
+ * bsa_bwd_noalloc's own; a word no launch has set up yet reads as 0, and
+ * nothing is allocated here.  The status is BSA_ERR_TIMEOUT /
+ * BSA_ERR_DEVICE when the word is non-zero. */
 BSA_API bsa_status bsa_get_device_error(bsa_stream stream, uint32_t* word);
 
 /* Time limit of one device-side wait, in nanoseconds (default 2e9).  Applies
