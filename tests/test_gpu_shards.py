@@ -7,7 +7,9 @@ is a lazy reference that may lag the true maximum, so m alone is not.  Rows
 with no visible key in a shard must come back exactly as o_acc = 0, l = 0,
 m = -inf.  The merge of the GPU shards must equal the unsharded forward of
 the oracle (O 2e-2, LSE 1e-5), and the merge kernel alone, fed the oracle's
-shards, must equal the oracle's merge.
+shards, must equal the oracle's merge.  At the benchmark's size (GQA 32/8
+causal, 8192, two shards) the merge is compared with the unsharded GPU
+forward in full and with the oracle on sampled rows.
 """
 import numpy as np
 import pytest
@@ -111,3 +113,16 @@ def test_two_shards_match_unsharded_forward_at_full_size():
     assert torch.all(p2[2][:, :, :h] == 0) and torch.all(torch.isneginf(p2[1][:, :, :h]))
     assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O
     assert (lse - lse_ref).abs().max().item() <= 1e-4
+    # and the merged result against the oracle on sampled rows of three
+    # heads (both shards' sides of the cut, the ends of the axis)
+    rng = np.random.default_rng(7)
+    mask = {"kind": "causal", "kv_len": S}
+    on, ln = o.float().cpu().numpy(), lse.cpu().numpy()
+    for hq in (0, 13, Hq - 1):
+        rows = np.array(sorted(set(rng.choice(S, size=120, replace=False).tolist())
+                               | {0, 127, h - 1, h, h + 1, S - 1}))
+        g = hq // (Hq // Hkv)
+        ro, rl = oatt.head_forward(f64(q[0, hq]), f64(k[0, g]), f64(v[0, g]), oatt.mask_rows_for(mask, 0),
+                                   1 / np.sqrt(D), rows=rows)
+        compare(f"merged O[0,{hq}] vs oracle", on[0, hq, rows], ro, TOL_O)
+        compare(f"merged LSE[0,{hq}] vs oracle", ln[0, hq, rows], rl, TOL_LSE)
