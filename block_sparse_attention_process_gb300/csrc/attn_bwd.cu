@@ -36,7 +36,10 @@
 //               half.  At a tile's end the same warps run the epilogue: bf16
 //               dK/dV through shared memory and tensor stores, dQ with
 //               32-byte stores.
-// All MMAs are 128 x 128 (full rate on sm_103a).
+// The dK/dV launch keeps each item's Q in three shared-memory stages and
+// its (dO, LSE, Dsum) in two: Q is what the next items need first (their
+// S^T), and with two stages its load had only the time of two GEMMs to
+// land.  All MMAs are 128 x 128 (full rate on sm_103a).
 #include <cmath>
 
 #include "internal.h"
