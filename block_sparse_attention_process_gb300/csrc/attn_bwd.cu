@@ -1179,7 +1179,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
         if (!dense_mask<kM>(p.mi.kind))
           query_interval(p.mi.kind, p.mi.left, p.mi.right, p.mi.chunk, static_cast<int64_t>(bi.z) + r, lo, hi);
       }
-      if (!mbar_wait_warp(&s.st_full, n & 1u, wc)) { ok = false; break; }
+      // the visibility bits (a dense mask's from memory) before the wait for the scores
       uint64_t allowed = ~0ull;
       if (label == 1) {
         if (dense_mask<kM>(p.mi.kind)) {
@@ -1189,6 +1189,7 @@ __global__ void __launch_bounds__(DkvShape<D>::kThreads, 1)
           allowed = interval_bits_64(static_cast<int64_t>(static_cast<int32_t>(bi.y)) + col0, lo, hi);
         }
       }
+      if (!mbar_wait_warp(&s.st_full, n & 1u, wc)) { ok = false; break; }
       // per-column statistics of this part's query rows
       const float4* lse4 = reinterpret_cast<const float4*>(&s.lse[st][col0]);
       // no branch joins while the loaded registers are in flight

@@ -604,10 +604,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint4 bi = s.binfo[slot];
       if (bi.x & kEnd) break;
       const uint32_t sb = n % kSBufs;
-      if (!mbar_wait_warp(&s.s_full[sb], (n / kSBufs) & 1u, wc)) { ok = false; break; }
-      // Released only now: the scores being ready means the K producer and
-      // the MMA warp have read this descriptor too.
-      if (lane == 0) mbar_arrive(&s.info_empty[slot]);
+      // A dense mask's visibility bits come from memory: they are loaded
+      // before the wait for the scores (they do not depend on them).  The
+      // other instantiations wait first (measured faster for them).
+      if constexpr (!kBits) {
+        if (!mbar_wait_warp(&s.s_full[sb], (n / kSBufs) & 1u, wc)) { ok = false; break; }
+      }
       const int32_t col = static_cast<int32_t>(bi.x & 0xFFFFu);
       const int32_t label = static_cast<int32_t>((bi.x >> 16) & 3u);
       const bool first = bi.x & kFirst, last = bi.x & kLast;
@@ -662,6 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if constexpr (kBits) {
+        if (!mbar_wait_warp(&s.s_full[sb], (n / kSBufs) & 1u, wc)) { ok = false; break; }
+      }
+      // Released only now: the scores being ready means the K producer and
+      // the MMA warp have read this descriptor too.
+      if (lane == 0) mbar_arrive(&s.info_empty[slot]);
       // no branch joins while the loaded registers are in flight
       tc_fence_after();
       uint32_t xu[kCols];
