@@ -539,7 +539,7 @@ def other_workloads(bsa, args, dev, pk, n_sms, flush, stream):
     return out
 
 
-def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws):
+def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws, keep=None):
     """Same metric through the public API from pinned host buffers: H2D of the
     step's inputs, mask compile, forward, backward, D2H of the gradients."""
     qh, kh, vh, doh = (t.pin_memory() for t in (q, k, v, do))
@@ -553,39 +553,72 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws):
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
 
     side = torch.cuda.Stream(device=dev)  # copies that overlap the kernels
+    cstream = torch.cuda.Stream(device=dev)  # the second mask compile
+    # The forward runs in two KV-head-aligned halves, so that the first
+    # half starts once its Q/K/V are in while the second half's are copied;
+    # dQ runs in four parts, each going back to the host while the next is
+    # computed.  The rowsum and dK/dV run once over all heads.  Heads are
+    # independent, so the results are those of single calls over all heads.
+    # (One part each when B > 1, where a head slice is not contiguous.)
+    G = w.Hq // w.Hkv
+
+    def parts(n):
+        n = n if (w.B == 1 and w.Hkv % n == 0) else 1
+        kv = w.Hkv // n
+        return [(slice(c * kv * G, (c + 1) * kv * G), slice(c * kv, (c + 1) * kv)) for c in range(n)]
+    fwd_parts, dq_parts = parts(2), parts(4)
 
     def one():
         main = torch.cuda.current_stream(dev)
-        # Q, K, V and then dO come in on the side stream while MaskInfo is
-        # compiled on the main one (a computable mask does not depend on the
-        # step's data; a dense one is copied in first, on the main stream);
-        # the forward waits for Q/K/V only, the backward for dO too
+        # Q, K, V (half by half) and then dO come in on the side stream while
+        # MaskInfo is compiled on the main one (a computable mask does not
+        # depend on the step's data; a dense one is copied in first, on the
+        # main stream)
         qd, kd, vd, dod = (torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (qh, kh, vh, doh))
         side.wait_stream(main)
+        qkv_in = []
         with torch.cuda.stream(side):
-            for d_, h_ in ((qd, qh), (kd, kh), (vd, vh)):
-                d_.copy_(h_, non_blocking=True)
-            qkv_in = torch.cuda.Event()
-            qkv_in.record(side)
+            for hs, gs in fwd_parts:
+                qd[:, hs].copy_(qh[:, hs], non_blocking=True)
+                kd[:, gs].copy_(kh[:, gs], non_blocking=True)
+                vd[:, gs].copy_(vh[:, gs], non_blocking=True)
+                qkv_in.append(torch.cuda.Event())
+                qkv_in[-1].record(side)
             dod.copy_(doh, non_blocking=True)
+            do_in = torch.cuda.Event()
+            do_in.record(side)
         dd = None if dense_hp is None else dense_hp.to(dev, non_blocking=True)
         info = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, **mask_kwargs(w))
-        dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, orientation="dkv", **mask_kwargs(w))
-        main.wait_event(qkv_in)
-        o, lse = bsa.fwd(qd, kd, vd, info)
-        main.wait_stream(side)
-        dsum = bsa.bwd_rowsum(o, dod)
-        dk, dv = bsa.bwd_dkv(qd, kd, vd, o, lse, dod, dsum, dkv)
-        # dK and dV go back to the host while dQ runs
+        o = torch.empty_like(qd)
+        lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+        dsum = torch.empty_like(lse)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        for ev, (hs, gs) in zip(qkv_in, fwd_parts):
+            main.wait_event(ev)
+            bsa.fwd(qd[:, hs], kd[:, gs], vd[:, gs], info, o=o[:, hs], lse=lse[:, hs])
+        # the dK/dV orientation compiles on its own stream while the forward
+        # runs (the compile returns once its MaskInfo is complete)
+        dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, orientation="dkv", stream=cstream,
+                               **mask_kwargs(w))
+        main.wait_stream(cstream)
+        main.wait_event(do_in)
+        bsa.bwd_rowsum(o, dod, dsum=dsum)
+        bsa.bwd_dkv(qd, kd, vd, o, lse, dod, dsum, dkv, dk=dk, dv=dv)
         side.wait_stream(main)
-        with torch.cuda.stream(side):
+        with torch.cuda.stream(side):  # dK and dV go back while dQ is computed
             outs_h[1].copy_(dk, non_blocking=True)
             outs_h[2].copy_(dv, non_blocking=True)
-        dq = bsa.bwd_dq(qd, kd, vd, o, lse, dod, dsum, info)
-        outs_h[0].copy_(dq, non_blocking=True)
+        for hs, gs in dq_parts:
+            bsa.bwd_dq(qd[:, hs], kd[:, gs], vd[:, gs], o[:, hs], lse[:, hs], dod[:, hs], dsum[:, hs], info,
+                       dq=dq[:, hs])
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                outs_h[0][:, hs].copy_(dq[:, hs], non_blocking=True)
+        main.wait_stream(side)
         torch.cuda.synchronize()
         info.destroy()
         dkv.destroy()
+        return outs_h
 
     for _ in range(max(1, args.warmup)):
         one()
@@ -595,10 +628,15 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws):
     for _ in range(n):
         one()
     dt = max_over_ranks((time.perf_counter() - t0) / n, dev)
+    if keep is not None:  # (the last step's gradients, for a check of the head-group split)
+        keep.extend(t.clone() for t in outs_h)
     return {"value": round(job_tflops(total_flop, dt, ws), 2), "unit": "TFLOP/s", "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "includes": "H2D Q/K/V and dO (side stream, during the mask compile and the forward), mask compile "
-                        "(fwd+dkv), fwd, rowsum, dK/dV, dQ, D2H dK/dV (side stream, during dQ) and dQ"}
+            "includes": "H2D Q/K/V (two KV-head halves) and dO (side stream, during the mask compile and the "
+                        "forward), mask compile (fwd orientation before the forward, dkv orientation on a third "
+                        "stream during it), fwd (per half), rowsum, dK/dV, dQ (four parts), D2H dK/dV and each dQ "
+                        "part (side stream, behind its launch)",
+            "parts": {"fwd": len(fwd_parts), "dq": len(dq_parts)}}
 
 
 ORACLE_ROWS = 1024   # query rows per oracle sample (one row chunk of one head)

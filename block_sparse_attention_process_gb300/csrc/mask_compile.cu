@@ -25,6 +25,9 @@
 // transposed mask.
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
 #include <vector>
 
 #include "internal.h"
@@ -49,6 +52,7 @@ struct Stats {
   int32_t n1;       // number of label-1 cells
   int32_t P;        // stack depth
 };
+static_assert(sizeof(Stats) % 4 == 0, "Stats is read back as 32-bit words");
 
 constexpr int64_t kInf = int64_t(1) << 40;
 
@@ -646,6 +650,64 @@ struct DevBuf {
   }
 };
 
+// Small read-backs (the counts and the row arrays) are written by a kernel
+// straight into mapped, pinned host memory.  A device-to-host copy is a
+// copy-engine transfer, and while other streams keep large host<->device
+// copies in flight it waits on them; stores from a kernel do not.  One
+// staging buffer for the process, grown on demand (an outgrown one stays
+// allocated: releasing pinned memory can synchronise the device), used
+// under a lock from the copy kernel's launch to the host's read.
+struct ReadBack {
+  void* host;
+  const void* dev;
+  size_t bytes;  // a multiple of 4
+};
+
+std::mutex g_stage_mu;
+uint32_t* g_stage = nullptr;
+size_t g_stage_words = 0;
+
+__global__ void words_to_host(uint32_t* __restrict__ dst, const uint32_t* __restrict__ src, int64_t n) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
+bsa_status read_back(cudaStream_t stream, std::initializer_list<ReadBack> parts) {
+  size_t words = 0;
+  for (const ReadBack& r : parts) words += r.bytes / 4;
+  std::lock_guard<std::mutex> lk(g_stage_mu);
+  cudaError_t e;
+  if (words > g_stage_words) {
+    const size_t cap = std::max<size_t>(std::max<size_t>(words, 2 * g_stage_words), 16384);
+    void* h = nullptr;
+    e = cudaHostAlloc(&h, cap * 4, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) return cuda_fail(e, "allocate the read-back buffer");
+    g_stage = static_cast<uint32_t*>(h);
+    g_stage_words = cap;
+  }
+  void* d = nullptr;
+  e = cudaHostGetDevicePointer(&d, g_stage, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "map the read-back buffer");
+  size_t off = 0;
+  for (const ReadBack& r : parts) {
+    const int64_t n = static_cast<int64_t>(r.bytes / 4);
+    if (n > 0)
+      words_to_host<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 152 * 4)), 256, 0, stream>>>(
+          static_cast<uint32_t*>(d) + off, static_cast<const uint32_t*>(r.dev), n);
+    off += static_cast<size_t>(n);
+  }
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "mask compile read-back");
+  off = 0;
+  for (const ReadBack& r : parts) {
+    if (r.bytes) std::memcpy(r.host, g_stage + off, r.bytes);
+    off += r.bytes / 4;
+  }
+  return BSA_OK;
+}
+
 }  // namespace
 
 bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opts, cudaStream_t stream,
@@ -774,8 +836,10 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   // one synchronisation: the grid width, the largest column, the counts
   // and the stack depth size the MaskInfo arrays
   Stats hs{};
-  BSA_CK(cudaMemcpyAsync(&hs, st, sizeof(Stats), cudaMemcpyDeviceToHost, stream), "read stats");
-  BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
+  {
+    const bsa_status rs = read_back(stream, {{&hs, st, sizeof(Stats)}});
+    if (rs != BSA_OK) return rs;
+  }
 
   if (dense && hs.n1 > 0) {
     BSA_ALLOC(info->partial, static_cast<size_t>(hs.P) * B * B);
@@ -839,13 +903,12 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
   // MaskInfo is complete
   info->row_len_h.resize(static_cast<size_t>(n_rows));
   info->row_order_h.resize(static_cast<size_t>(n_rows));
-  BSA_CK(cudaMemcpyAsync(info->row_len_h.data(), info->row_len, n_rows * sizeof(int32_t), cudaMemcpyDeviceToHost,
-                         stream),
-         "copy row_len");
-  BSA_CK(cudaMemcpyAsync(info->row_order_h.data(), info->row_order, n_rows * sizeof(int32_t),
-                         cudaMemcpyDeviceToHost, stream),
-         "copy row_order");
-  BSA_CK(cudaStreamSynchronize(stream), "mask compile sync");
+  {
+    const size_t nb = static_cast<size_t>(n_rows) * sizeof(int32_t);
+    const bsa_status rs = read_back(stream, {{info->row_len_h.data(), info->row_len, nb},
+                                             {info->row_order_h.data(), info->row_order, nb}});
+    if (rs != BSA_OK) return rs;
+  }
 #undef BSA_ALLOC
 #undef BSA_CK
   guard.keep = true;

@@ -7,9 +7,8 @@
 // CTA with the least work so far) evens the CTAs' totals out, so short
 // tiles fill the gaps left by the long ones.
 #include <algorithm>
-#include <functional>
-#include <queue>
-#include <utility>
+#include <cstddef>
+#include <iterator>
 
 #include "internal.h"
 
@@ -62,25 +61,48 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
     std::stable_sort(tiles.begin(), tiles.end(), [](const T& x, const T& y) { return x.n > y.n; });
   }
   // greedy; cost in eighths of a block, with a per-tile overhead of about
-  // one and a half blocks
-  std::vector<std::vector<int4>> lists(static_cast<size_t>(grid));
-  using Load = std::pair<int64_t, int32_t>;  // (work so far, CTA): ties go to the lower CTA
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-  for (int32_t c = 0; c < grid; ++c) heap.push({0, c});
-  for (const T& t : tiles) {
-    Load top = heap.top();
-    heap.pop();
-    lists[static_cast<size_t>(top.second)].push_back(make_int4(t.i, t.n, t.bg, t.sp));
-    top.first += 8 * static_cast<int64_t>(t.n) + 12;
-    heap.push(top);
+  // one and a half blocks.  The CTAs are kept sorted by key = (work so far)
+  // << 16 | CTA, so the smallest key is the least-loaded CTA, ties going to
+  // the lower index.  The tiles come in runs of equal size (longest first);
+  // within a run the keys taken out grow, so the updated keys form a second
+  // sorted list, merged back when the run ends: linear work per run instead
+  // of a heap operation per tile, with the same assignment.
+  if (grid > 0xFFFF) return fail(BSA_ERR_UNSUPPORTED, "tile schedule grid above 65535");
+  std::vector<uint64_t> keys(static_cast<size_t>(grid)), upd, merged;
+  for (int32_t c = 0; c < grid; ++c) keys[static_cast<size_t>(c)] = static_cast<uint64_t>(c);
+  upd.reserve(static_cast<size_t>(grid));
+  merged.reserve(static_cast<size_t>(grid));
+  std::vector<int32_t> owner(tiles.size()), slot(tiles.size()), count(static_cast<size_t>(grid), 0);
+  for (size_t k = 0; k < tiles.size();) {
+    const int32_t n = tiles[k].n;
+    const uint64_t add = static_cast<uint64_t>(8 * static_cast<int64_t>(n) + 12) << 16;
+    size_t ki = 0, ui = 0;
+    upd.clear();
+    for (; k < tiles.size() && tiles[k].n == n; ++k) {
+      const bool from_keys = ki < keys.size() && (ui == upd.size() || keys[ki] < upd[ui]);
+      const uint64_t top = from_keys ? keys[ki++] : upd[ui++];
+      const int32_t c = static_cast<int32_t>(top & 0xFFFFu);
+      owner[k] = c;
+      slot[k] = count[static_cast<size_t>(c)]++;
+      upd.push_back(top + add);
+    }
+    if (upd.size() - ui <= 4) {  // a short run: insert its few keys
+      keys.erase(keys.begin(), keys.begin() + static_cast<std::ptrdiff_t>(ki));
+      for (size_t j = ui; j < upd.size(); ++j) keys.insert(std::upper_bound(keys.begin(), keys.end(), upd[j]), upd[j]);
+    } else {
+      merged.clear();
+      std::merge(keys.begin() + static_cast<std::ptrdiff_t>(ki), keys.end(),
+                 upd.begin() + static_cast<std::ptrdiff_t>(ui), upd.end(), std::back_inserter(merged));
+      keys.swap(merged);
+    }
   }
-  size_t longest = 0;
-  for (const auto& l : lists) longest = std::max(longest, l.size());
-  const int32_t st = static_cast<int32_t>(longest) + 1;  // room for the end mark
+  int32_t longest = 0;
+  for (int32_t c : count) longest = std::max(longest, c);
+  const int32_t st = longest + 1;  // room for the end mark
   std::vector<int4> flat(static_cast<size_t>(grid) * st, make_int4(0, -1, 0, 0));
-  for (int32_t c = 0; c < grid; ++c)
-    std::copy(lists[static_cast<size_t>(c)].begin(), lists[static_cast<size_t>(c)].end(),
-              flat.begin() + static_cast<size_t>(c) * st);
+  for (size_t k = 0; k < tiles.size(); ++k)
+    flat[static_cast<size_t>(owner[k]) * st + static_cast<size_t>(slot[k])] =
+        make_int4(tiles[k].i, tiles[k].n, tiles[k].bg, tiles[k].sp);
   // stream-ordered upload (no synchronisation with earlier work on the
   // device), from a host copy that lives as long as the schedule
   bsa_mask_info::Schedule sc;

@@ -27,8 +27,8 @@
  *   128.
  * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *   is asynchronous on that stream except bsa_mask_compile (which
- *   synchronises once to learn the grid width and the stack size),
- *   bsa_mask_info_destroy and bsa_get_device_error.
+ *   synchronises `stream` to learn the grid width and the stack size, and
+ *   before it returns), bsa_mask_info_destroy and bsa_get_device_error.
  * - Calls return a status; none throws.  On failure bsa_last_error()
  *   returns a message for the calling thread.  Argument errors are found on
  *   the host before anything is launched.
@@ -127,8 +127,12 @@ typedef struct {
  * complete on return, and the attention kernels read it without waiting for
  * earlier work on their stream.  Its device memory (and the compile's
  * scratch) comes from a stream-ordered memory pool the library keeps per
- * device, so no step of the compile synchronises the whole device.  *out
- * receives a new handle on success and is untouched on failure. */
+ * device, so no step of the compile synchronises the whole device.  The
+ * counts and row arrays the host needs come back through a pinned, mapped
+ * host buffer that a kernel writes (no copy-engine transfer), so the compile
+ * does not wait behind large host<->device copies other streams have in
+ * flight.  *out receives a new handle on success and is untouched on
+ * failure. */
 BSA_API bsa_status bsa_mask_compile(const bsa_mask_spec* spec, const bsa_mask_opts* opts, bsa_stream stream,
                             bsa_mask_info** out);
 BSA_API bsa_status bsa_mask_info_view(const bsa_mask_info* info, bsa_mask_info_desc* out);
