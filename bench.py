@@ -596,13 +596,14 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws, keep=None):
         for ev, (hs, gs) in zip(qkv_in, fwd_parts):
             main.wait_event(ev)
             bsa.fwd(qd[:, hs], kd[:, gs], vd[:, gs], info, o=o[:, hs], lse=lse[:, hs])
-        # the dK/dV orientation compiles on its own stream while the forward
-        # runs (the compile returns once its MaskInfo is complete)
+        main.wait_event(do_in)
+        bsa.bwd_rowsum(o, dod, dsum=dsum)
+        # the dK/dV orientation compiles on its own stream once the forward
+        # and the rowsum are queued (the compile returns when its MaskInfo is
+        # complete)
         dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, orientation="dkv", stream=cstream,
                                **mask_kwargs(w))
         main.wait_stream(cstream)
-        main.wait_event(do_in)
-        bsa.bwd_rowsum(o, dod, dsum=dsum)
         bsa.bwd_dkv(qd, kd, vd, o, lse, dod, dsum, dkv, dk=dk, dv=dv)
         side.wait_stream(main)
         with torch.cuda.stream(side):  # dK and dV go back while dQ is computed
@@ -634,8 +635,8 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws, keep=None):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "includes": "H2D Q/K/V (two KV-head halves) and dO (side stream, during the mask compile and the "
                         "forward), mask compile (fwd orientation before the forward, dkv orientation on a third "
-                        "stream during it), fwd (per half), rowsum, dK/dV, dQ (four parts), D2H dK/dV and each dQ "
-                        "part (side stream, behind its launch)",
+                        "stream once the forward and rowsum are queued), fwd (per half), rowsum, dK/dV, dQ (four "
+                        "parts), D2H dK/dV and each dQ part (side stream, behind its launch)",
             "parts": {"fwd": len(fwd_parts), "dq": len(dq_parts)}}
 
 
