@@ -89,6 +89,9 @@ SIGNATURES = {
     "bsa_set_wait_limit_ns": (C.c_int, [C.c_uint64]),
     "bsa_debug_wait_timeout": (C.c_int, [C.c_void_p]),
     "bsa_debug_selfcheck": (C.c_int, [C.c_void_p]),
+    "bsa_debug_tile_schedule": (C.c_int, [C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.c_int32, C.c_int32,
+                                          C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                          C.POINTER(C.c_int32), C.c_int32, C.POINTER(C.c_int32)]),
     "bsa_status_string": (C.c_char_p, [C.c_int]),
     "bsa_last_error": (C.c_char_p, []),
     "bsa_version": (C.c_char_p, []),

@@ -264,6 +264,28 @@ bsa_status bsa_debug_selfcheck(bsa_stream stream) {
   return debug_selfcheck_launch(static_cast<cudaStream_t>(stream));
 }
 
+bsa_status bsa_debug_tile_schedule(const int32_t* row_len, const int32_t* row_order, int32_t rows, int32_t heads,
+                                   int32_t n_b, int32_t n_g, int32_t group, int32_t splits, int32_t grid,
+                                   int32_t* out, int32_t cap, int32_t* stride) {
+  if (!row_len || !row_order || !out || !stride) return fail(BSA_ERR_INVALID_ARG, "null pointer");
+  std::vector<int4> flat;
+  int32_t st = 0;
+  const bsa_status s = schedule_lists(row_len, row_order, rows, heads, n_b, n_g, group, splits, grid, &flat, &st);
+  if (s != BSA_OK) return s;
+  *stride = st;
+  if (cap < st) return fail(BSA_ERR_INVALID_ARG, "cap is below the schedule's stride");
+  for (int32_t c = 0; c < grid; ++c)
+    for (int32_t k = 0; k < cap; ++k) {
+      const int4 e = k < st ? flat[static_cast<size_t>(c) * st + k] : make_int4(0, -1, 0, 0);
+      int32_t* o = out + (static_cast<size_t>(c) * cap + k) * 4;
+      o[0] = e.x;
+      o[1] = e.y;
+      o[2] = e.z;
+      o[3] = e.w;
+    }
+  return BSA_OK;
+}
+
 bsa_status bsa_get_device_error(bsa_stream stream, uint32_t* word) {
   if (!word) return fail(BSA_ERR_INVALID_ARG, "word is null");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -99,6 +99,11 @@ uint32_t* noalloc_error_word_if_set();
 // Built on the first launch of a (n_b, n_g, group, splits, grid, device)
 // and cached in the MaskInfo; `stream` (the launch's) is ordered after its
 // upload.
+// The host part of a tile schedule: CTA c's entries {row, blocks, b*n_g + g,
+// split} at flat[c*stride ..], each list closed by an entry with blocks -1.
+bsa_status schedule_lists(const int32_t* row_len, const int32_t* row_order, int32_t rows, int32_t heads,
+                          int32_t n_b, int32_t n_g, int32_t group, int32_t splits, int32_t grid,
+                          std::vector<int4>* flat, int32_t* stride);
 bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t splits,
                          int32_t grid, cudaStream_t stream, const int4** out, int32_t* stride);
 

@@ -14,22 +14,9 @@
 
 namespace bsa {
 
-bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t splits,
-                         int32_t grid, cudaStream_t stream, const int4** out, int32_t* stride) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  std::lock_guard<std::mutex> lk(info->sched_mu);
-  for (const auto& sc : info->schedules)
-    if (sc.n_b == n_b && sc.n_g == n_g && sc.group == group && sc.splits == splits && sc.grid == grid &&
-        sc.device == dev) {
-      e = cudaStreamWaitEvent(stream, sc.ready, 0);
-      if (e != cudaSuccess) return cuda_fail(e, "wait for the tile schedule upload");
-      *out = sc.dev;
-      *stride = sc.stride;
-      return BSA_OK;
-    }
-  const int32_t rows = info->rows;
+bsa_status schedule_lists(const int32_t* row_len, const int32_t* row_order, int32_t rows, int32_t heads,
+                          int32_t n_b, int32_t n_g, int32_t group, int32_t splits, int32_t grid,
+                          std::vector<int4>* flat, int32_t* stride) {
   if (grid <= 0 || rows <= 0 || n_b <= 0 || n_g <= 0 || group <= 0 || splits <= 0 || group % splits)
     return fail(BSA_ERR_INVALID_ARG, "empty tile schedule");
   const int32_t gs = group / splits;  // mask heads of one split
@@ -39,11 +26,11 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
   };
   std::vector<T> tiles;
   tiles.reserve(static_cast<size_t>(rows) * n_b * n_g);
-  if (info->heads == 1) {
+  if (heads == 1) {
     // rows by decreasing length (row_order), each for every (b, g)
     for (int32_t rank = 0; rank < rows; ++rank) {
-      const int32_t i = info->row_order_h[static_cast<size_t>(rank)];
-      const int32_t n = info->row_len_h[static_cast<size_t>(i)] * gs;
+      const int32_t i = row_order[rank];
+      const int32_t n = row_len[i] * gs;
       for (int32_t bg = 0; bg < n_b * n_g; ++bg)
         for (int32_t sp = 0; sp < splits; ++sp) tiles.push_back({i, n, bg, sp});
     }
@@ -55,7 +42,7 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
         for (int32_t sp = 0; sp < splits; ++sp) {
           int32_t n = 0;
           for (int32_t gh = sp * gs; gh < (sp + 1) * gs; ++gh)
-            n += info->row_len_h[static_cast<size_t>((g * group + gh) * rows + i)];
+            n += row_len[static_cast<size_t>(g * group + gh) * rows + i];
           for (int32_t b = 0; b < n_b; ++b) tiles.push_back({i, n, b * n_g + g, sp});
         }
     std::stable_sort(tiles.begin(), tiles.end(), [](const T& x, const T& y) { return x.n > y.n; });
@@ -99,10 +86,36 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
   int32_t longest = 0;
   for (int32_t c : count) longest = std::max(longest, c);
   const int32_t st = longest + 1;  // room for the end mark
-  std::vector<int4> flat(static_cast<size_t>(grid) * st, make_int4(0, -1, 0, 0));
+  flat->assign(static_cast<size_t>(grid) * st, make_int4(0, -1, 0, 0));
   for (size_t k = 0; k < tiles.size(); ++k)
-    flat[static_cast<size_t>(owner[k]) * st + static_cast<size_t>(slot[k])] =
+    (*flat)[static_cast<size_t>(owner[k]) * st + static_cast<size_t>(slot[k])] =
         make_int4(tiles[k].i, tiles[k].n, tiles[k].bg, tiles[k].sp);
+  *stride = st;
+  return BSA_OK;
+}
+
+bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, int32_t group, int32_t splits,
+                         int32_t grid, cudaStream_t stream, const int4** out, int32_t* stride) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(info->sched_mu);
+  for (const auto& sc : info->schedules)
+    if (sc.n_b == n_b && sc.n_g == n_g && sc.group == group && sc.splits == splits && sc.grid == grid &&
+        sc.device == dev) {
+      e = cudaStreamWaitEvent(stream, sc.ready, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "wait for the tile schedule upload");
+      *out = sc.dev;
+      *stride = sc.stride;
+      return BSA_OK;
+    }
+  std::vector<int4> flat;
+  int32_t st = 0;
+  {
+    const bsa_status ls = schedule_lists(info->row_len_h.data(), info->row_order_h.data(), info->rows, info->heads,
+                                         n_b, n_g, group, splits, grid, &flat, &st);
+    if (ls != BSA_OK) return ls;
+  }
   // stream-ordered upload (no synchronisation with earlier work on the
   // device), from a host copy that lives as long as the schedule
   bsa_mask_info::Schedule sc;

@@ -340,6 +340,24 @@ BSA_API bsa_status bsa_debug_wait_timeout(bsa_stream stream);
  * range-checked build reports what it finds. */
 BSA_API bsa_status bsa_debug_selfcheck(bsa_stream stream);
 
+/* The launch-time tile schedule of the persistent attention launches, as
+ * they build it on the host (a testing aid: no device work, no GPU needed).
+ * Inputs as a MaskInfo holds them: row_len[heads * rows] (non-empty blocks
+ * per mask row) and row_order[rows] (rows by decreasing length; read only
+ * when heads == 1).  Tiles are (batch of n_b, group g of n_g, mask row,
+ * split) with `group` mask heads per group split in `splits` (the forward
+ * and dQ launches: n_g = Hq, group = splits = 1; dK/dV: n_g = Hkv, group =
+ * Hq / Hkv).  They are assigned longest first, each to the CTA of the
+ * `grid` with the least work so far (ties to the lower index; a tile of n
+ * blocks costs 8n + 12).  Writes CTA c's list at out[(c * cap + k) * 4 +
+ * {0..3}] = {row, blocks, b * n_g + g, split}, closed by an entry with
+ * blocks = -1 and padded with such entries, and *stride = the longest list
+ * + 1; BSA_ERR_INVALID_ARG (with *stride set) when cap < *stride. */
+BSA_API bsa_status bsa_debug_tile_schedule(const int32_t* row_len, const int32_t* row_order, int32_t rows,
+                                           int32_t heads, int32_t n_b, int32_t n_g, int32_t group,
+                                           int32_t splits, int32_t grid, int32_t* out, int32_t cap,
+                                           int32_t* stride);
+
 BSA_API const char* bsa_status_string(bsa_status s);
 BSA_API const char* bsa_last_error(void);
 /* Library version, e.g. "0.1.0". */
