@@ -92,7 +92,14 @@ __device__ __forceinline__ void row_interval(const MaskParams& p, int64_t r, int
 // Each block row of a computable mask allows one interval per element row,
 // so counting the overlap of that interval with the block's columns decides
 // any()/all() exactly.  One CTA (128 threads, one per element row) per cell.
-__global__ void classify_computable(MaskParams p, int8_t* __restrict__ labels, int64_t n_cells) {
+// The same launch clears the grid-wide counts (which the row pass, the next
+// launch, accumulates) and writes q_sequence (the identity).
+__global__ void classify_computable(MaskParams p, int8_t* __restrict__ labels, int64_t n_cells, Stats* st,
+                                    int32_t* __restrict__ q_sequence) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *st = Stats{};
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.q_len;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    q_sequence[i] = static_cast<int32_t>(i);
   for (int64_t cell = blockIdx.x; cell < n_cells; cell += gridDim.x) {
     const int c = static_cast<int>(cell % p.nC);
     const int r = static_cast<int>((cell / p.nC) % p.nR);
@@ -578,6 +585,24 @@ struct ArrayOut {  // exclusive prefix sums in place of the values
   __device__ __forceinline__ void operator()(int64_t i, int, int pos) const { a[i] = pos; }
 };
 
+// Ascending bitonic sort of kChunk keys in shared memory, one per thread.
+__device__ __forceinline__ void bitonic_sort(unsigned long long* key, int t) {
+  __syncthreads();
+  for (int k = 2; k <= kChunk; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int partner = t ^ j;
+      if (partner > t) {
+        const unsigned long long a = key[t], b = key[partner];
+        const bool up = (t & k) == 0;
+        if ((a > b) == up) {
+          key[t] = b;
+          key[partner] = a;
+        }
+      }
+      __syncthreads();
+    }
+}
+
 __global__ void __launch_bounds__(kChunk) order_place(const int32_t* __restrict__ row_len, int64_t n_rows,
                                                      int32_t max_len, int64_t n_chunks,
                                                      const int32_t* __restrict__ offs, int32_t* __restrict__ order) {
@@ -588,20 +613,7 @@ __global__ void __launch_bounds__(kChunk) order_place(const int32_t* __restrict_
     const int64_t i = c * kChunk + t;
     key[t] = i < n_rows ? (static_cast<unsigned long long>(max_len - row_len[i]) << 32) | static_cast<unsigned>(t)
                         : ~0ull;
-    __syncthreads();
-    for (int k = 2; k <= kChunk; k <<= 1)
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const int partner = t ^ j;
-        if (partner > t) {
-          const unsigned long long a = key[t], b = key[partner];
-          const bool up = (t & k) == 0;
-          if ((a > b) == up) {
-            key[t] = b;
-            key[partner] = a;
-          }
-        }
-        __syncthreads();
-      }
+    bitonic_sort(key, t);
     const unsigned long long me = key[t];
     const uint32_t bucket = static_cast<uint32_t>(me >> 32);
     start[t] = (t == 0 || static_cast<uint32_t>(key[t - 1] >> 32) != bucket) ? t : 0;
@@ -618,6 +630,18 @@ __global__ void __launch_bounds__(kChunk) order_place(const int32_t* __restrict_
           static_cast<int32_t>(c * kChunk + static_cast<int64_t>(me & 0xFFFFFFFFull));
     __syncthreads();
   }
+}
+
+// The same order for at most kChunk rows in one CTA: sorted by (bucket,
+// row), a row's place in the sorted keys is its place in the order.
+__global__ void __launch_bounds__(kChunk) order_small(const int32_t* __restrict__ row_len, int32_t n_rows,
+                                                     int32_t max_len, int32_t* __restrict__ order) {
+  __shared__ unsigned long long key[kChunk];
+  const int t = threadIdx.x;
+  key[t] = t < n_rows ? (static_cast<unsigned long long>(max_len - row_len[t]) << 32) | static_cast<unsigned>(t)
+                      : ~0ull;
+  bitonic_sort(key, t);
+  if (t < n_rows) order[t] = static_cast<int32_t>(key[t] & 0xFFFFFFFFull);
 }
 
 // BSA_DEDUP_HASH_BITS=n (0..63) keeps only the low n bits of every block
@@ -667,13 +691,23 @@ std::mutex g_stage_mu;
 uint32_t* g_stage = nullptr;
 size_t g_stage_words = 0;
 
-__global__ void words_to_host(uint32_t* __restrict__ dst, const uint32_t* __restrict__ src, int64_t n) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    dst[i] = src[i];
+constexpr int kMaxReadBack = 2;
+struct WordCopies {
+  uint32_t* dst[kMaxReadBack];
+  const uint32_t* src[kMaxReadBack];
+  int64_t n[kMaxReadBack];
+  int count;
+};
+
+__global__ void words_to_host(WordCopies w) {
+  for (int k = 0; k < w.count; ++k)
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < w.n[k];
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      w.dst[k][i] = w.src[k][i];
 }
 
 bsa_status read_back(cudaStream_t stream, std::initializer_list<ReadBack> parts) {
+  if (parts.size() > static_cast<size_t>(kMaxReadBack)) return fail(BSA_ERR_UNSUPPORTED, "too many read-back parts");
   size_t words = 0;
   for (const ReadBack& r : parts) words += r.bytes / 4;
   std::lock_guard<std::mutex> lk(g_stage_mu);
@@ -689,14 +723,20 @@ bsa_status read_back(cudaStream_t stream, std::initializer_list<ReadBack> parts)
   void* d = nullptr;
   e = cudaHostGetDevicePointer(&d, g_stage, 0);
   if (e != cudaSuccess) return cuda_fail(e, "map the read-back buffer");
+  // one launch copies every part
+  WordCopies w{};
   size_t off = 0;
+  int64_t most = 0;
   for (const ReadBack& r : parts) {
-    const int64_t n = static_cast<int64_t>(r.bytes / 4);
-    if (n > 0)
-      words_to_host<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 152 * 4)), 256, 0, stream>>>(
-          static_cast<uint32_t*>(d) + off, static_cast<const uint32_t*>(r.dev), n);
-    off += static_cast<size_t>(n);
+    w.dst[w.count] = static_cast<uint32_t*>(d) + off;
+    w.src[w.count] = static_cast<const uint32_t*>(r.dev);
+    w.n[w.count] = static_cast<int64_t>(r.bytes / 4);
+    most = std::max(most, w.n[w.count]);
+    off += r.bytes / 4;
+    ++w.count;
   }
+  if (most > 0)
+    words_to_host<<<static_cast<unsigned>(std::min<int64_t>((most + 255) / 256, 152 * 4)), 256, 0, stream>>>(w);
   e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "mask compile read-back");
@@ -752,7 +792,8 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
 
   BSA_ALLOC(labels.p, n_cells);
   BSA_ALLOC(stats.p, sizeof(Stats));
-  BSA_CK(cudaMemsetAsync(stats.p, 0, sizeof(Stats), stream), "clear stats");
+  // (a computable mask's classifier clears the counts itself)
+  if (dense) BSA_CK(cudaMemsetAsync(stats.p, 0, sizeof(Stats), stream), "clear stats");
 
   auto* info = new bsa_mask_info();
   struct Guard {
@@ -784,7 +825,8 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
     classify_dense<<<grid_cells, 256, 0, stream>>>(p, static_cast<int8_t*>(labels.p),
                                                   static_cast<uint64_t*>(hashes.p), n_cells);
   } else {
-    classify_computable<<<grid_cells, B, 0, stream>>>(p, static_cast<int8_t*>(labels.p), n_cells);
+    classify_computable<<<grid_cells, B, 0, stream>>>(p, static_cast<int8_t*>(labels.p), n_cells, st,
+                                                       info->q_sequence);
   }
   BSA_CK(cudaGetLastError(), "classify launch");
   row_pass<<<static_cast<unsigned>((n_rows + 127) / 128), 128, 0, stream>>>(
@@ -876,10 +918,16 @@ bsa_status mask_compile_impl(const bsa_mask_spec* spec, const bsa_mask_opts* opt
         info->block_mask, info->data_next, info->data_next_bytes, info->mask_next, info->mask_next_bytes);
     BSA_CK(cudaGetLastError(), "write_rows launch");
   }
-  iota_i32<<<static_cast<unsigned>((p.q_len + 255) / 256), 256, 0, stream>>>(info->q_sequence, p.q_len);
-  BSA_CK(cudaGetLastError(), "iota launch");
-  // rows by decreasing length (stable counting sort)
-  {
+  if (dense) {
+    iota_i32<<<static_cast<unsigned>((p.q_len + 255) / 256), 256, 0, stream>>>(info->q_sequence, p.q_len);
+    BSA_CK(cudaGetLastError(), "iota launch");
+  }
+  // rows by decreasing length (stable counting sort; up to kChunk rows, one
+  // CTA sorting (bucket, row) keys)
+  if (n_rows <= kChunk) {
+    order_small<<<1, kChunk, 0, stream>>>(info->row_len, static_cast<int32_t>(n_rows), p.nC, info->row_order);
+    BSA_CK(cudaGetLastError(), "row order launch");
+  } else {
     const int64_t r_chunks = (n_rows + kChunk - 1) / kChunk;
     const int64_t n_cnt = static_cast<int64_t>(p.nC + 1) * r_chunks;
     BSA_ALLOC(hist.p, n_cnt * sizeof(int32_t));
