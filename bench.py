@@ -589,6 +589,12 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws, keep=None):
             do_in.record(side)
         dd = None if dense_hp is None else dense_hp.to(dev, non_blocking=True)
         info = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, **mask_kwargs(w))
+        # the dK/dV orientation right after, while the SMs are free (the
+        # forward waits for its inputs anyway); on its own stream, each
+        # compile returning once its MaskInfo is complete
+        cstream.wait_stream(main)
+        dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, orientation="dkv", stream=cstream,
+                               **mask_kwargs(w))
         o = torch.empty_like(qd)
         lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
         dsum = torch.empty_like(lse)
@@ -598,11 +604,6 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws, keep=None):
             bsa.fwd(qd[:, hs], kd[:, gs], vd[:, gs], info, o=o[:, hs], lse=lse[:, hs])
         main.wait_event(do_in)
         bsa.bwd_rowsum(o, dod, dsum=dsum)
-        # the dK/dV orientation compiles on its own stream once the forward
-        # and the rowsum are queued (the compile returns when its MaskInfo is
-        # complete)
-        dkv = bsa.mask_compile(w.mask.kind, w.S, w.S, dense=dd, orientation="dkv", stream=cstream,
-                               **mask_kwargs(w))
         main.wait_stream(cstream)
         bsa.bwd_dkv(qd, kd, vd, o, lse, dod, dsum, dkv, dk=dk, dv=dv)
         side.wait_stream(main)
@@ -634,8 +635,8 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws, keep=None):
     return {"value": round(job_tflops(total_flop, dt, ws), 2), "unit": "TFLOP/s", "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "includes": "H2D Q/K/V (two KV-head halves) and dO (side stream, during the mask compile and the "
-                        "forward), mask compile (fwd orientation before the forward, dkv orientation on a third "
-                        "stream once the forward and rowsum are queued), fwd (per half), rowsum, dK/dV, dQ (four "
+                        "forward), mask compile (both orientations before the forward, the dkv one on a third "
+                        "stream), fwd (per half), rowsum, dK/dV, dQ (four "
                         "parts), D2H dK/dV and each dQ part (side stream, behind its launch)",
             "parts": {"fwd": len(fwd_parts), "dq": len(dq_parts)}}
 
