@@ -539,7 +539,7 @@ def other_workloads(bsa, args, dev, pk, n_sms, flush, stream):
     return out
 
 
-def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws, keep=None):
+def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws):
     """Same metric through the public API from pinned host buffers: H2D of the
     step's inputs, mask compile, forward, backward, D2H of the gradients."""
     qh, kh, vh, doh = (t.pin_memory() for t in (q, k, v, do))
@@ -630,8 +630,6 @@ def run_e2e(bsa, w, q, k, v, do, dense_h, dev, args, total_flop, ws, keep=None):
     for _ in range(n):
         one()
     dt = max_over_ranks((time.perf_counter() - t0) / n, dev)
-    if keep is not None:  # (the last step's gradients, for a check of the head-group split)
-        keep.extend(t.clone() for t in outs_h)
     return {"value": round(job_tflops(total_flop, dt, ws), 2), "unit": "TFLOP/s", "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "includes": "H2D Q/K/V (two KV-head halves) and dO (side stream, during the mask compile and the "
