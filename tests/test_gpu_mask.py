@@ -223,3 +223,21 @@ def test_many_partial_blocks_with_duplicates_across_chunks():
         ref, got = compile_both("dense", nq * 128, nk * 128, dense=m, orientation=o)
         assert ref.n_partial > 1024 and got["num_partial"] == 40
         assert_same(ref, got)
+
+
+@pytest.mark.parametrize("orientation", ["fwd", "dkv"])
+@pytest.mark.parametrize("heads", [1, 3])
+def test_rectangular_dense_bit_exact(orientation, heads):
+    """S_q != S_kv (384 x 896): rows and columns have different extents in
+    each orientation; a query block with no visible key and a key block no
+    query sees are planted."""
+    need_gpu()
+    rng = np.random.default_rng(17 + heads)
+    m = (rng.random((heads, 384, 896)) < 0.3).astype(np.uint8)
+    m[:, 128:256, :] = 0
+    m[:, :, 768:] = 0
+    m[:, 256:, 128:256] = 1  # full blocks
+    dense = m if heads > 1 else m[0]
+    for shrink in (True, False):
+        ref, got = compile_both("dense", 384, 896, dense=dense, orientation=orientation, shrink=shrink)
+        assert_same(ref, got)
