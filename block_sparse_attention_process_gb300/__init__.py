@@ -100,6 +100,8 @@ class MaskInfo:
             "partial_mask_blocks": None if not d.partial_mask_blocks else
             _view(d.partial_mask_blocks, (d.num_partial, 128, 128), torch.uint8),
             "q_sequence": _view(d.q_sequence, (d.q_len,), torch.int32),
+            "row_len": _view(d.row_len, (d.heads * d.rows,), torch.int32),
+            "row_order": _view(d.row_order, (d.heads * d.rows,), torch.int32),
         }
         return out
 

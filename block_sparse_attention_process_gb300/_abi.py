@@ -39,7 +39,8 @@ class MaskInfoDesc(C.Structure):
                 ("heads", C.c_int32), ("rows", C.c_int32), ("width", C.c_int32), ("cols", C.c_int32),
                 ("num_partial", C.c_int64), ("n_empty", C.c_int64), ("n_partial", C.c_int64),
                 ("n_full", C.c_int64), ("kind", C.c_int32), ("orientation", C.c_int32),
-                ("shrink", C.c_int32), ("q_len", C.c_int64), ("kv_len", C.c_int64)]
+                ("shrink", C.c_int32), ("q_len", C.c_int64), ("kv_len", C.c_int64),
+                ("row_len", C.c_void_p), ("row_order", C.c_void_p)]
 
 
 class FwdArgs(C.Structure):

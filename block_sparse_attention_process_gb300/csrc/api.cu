@@ -369,6 +369,8 @@ bsa_status bsa_mask_info_view(const bsa_mask_info* info, bsa_mask_info_desc* out
   out->shrink = info->shrink;
   out->q_len = info->q_len;
   out->kv_len = info->kv_len;
+  out->row_len = info->row_len;
+  out->row_order = info->row_order;
   return BSA_OK;
 }
 

@@ -117,6 +117,11 @@ typedef struct {
   int64_t n_empty, n_partial, n_full; /* block counts over the unshrunk grid, all heads */
   int32_t kind, orientation, shrink;
   int64_t q_len, kv_len;
+  /* the library's own row arrays (beside MaskInfo proper, from which the
+   * launches build their tile schedules): non-empty blocks per mask row,
+   * and the rows by decreasing length, ties in increasing row order */
+  const int32_t* row_len;             /* [heads * rows] */
+  const int32_t* row_order;           /* [heads * rows] */
 } bsa_mask_info_desc;
 
 /* Compile a mask into MaskInfo ("What is MaskInfo in splash attention?",

@@ -241,3 +241,31 @@ def test_rectangular_dense_bit_exact(orientation, heads):
     for shrink in (True, False):
         ref, got = compile_both("dense", 384, 896, dense=dense, orientation=orientation, shrink=shrink)
         assert_same(ref, got)
+
+
+@pytest.mark.parametrize("orientation", ["fwd", "dkv"])
+@pytest.mark.parametrize("case", ["causal_8192", "local_8192", "per_head_64x2048", "per_head_72x2048"])
+def test_row_lengths_and_order(case, orientation):
+    """The library's own row arrays, from which the launches build their tile
+    schedules: row_len is each mask row's number of non-empty blocks (the
+    oracle's count), row_order the rows by decreasing length, ties in
+    increasing row order.  Up to 1024 rows one CTA sorts them (64 per-head
+    masks of 16 block rows: exactly 1024); above that a counting sort over
+    1024-row chunks does (72 x 16 = 1152 rows)."""
+    need_gpu()
+    import block_sparse_attention_process_gb300 as bsa
+    kind, dense, S, kw, okw = "dense", None, 2048, {}, {}
+    if case == "causal_8192":
+        kind, S = "causal", 8192
+    elif case == "local_8192":
+        kind, S, kw, okw = "local", 8192, dict(local_left=1024, local_right=0), dict(left=1024, right=0)
+    else:
+        dense = per_head_dense_mask(int(case.split("_")[2].split("x")[0]), S)
+    ref = omi.compile_mask_info(kind, S, S, dense=dense, orientation=orientation, **okw)
+    dd = None if dense is None else torch.from_numpy(dense).cuda()
+    info = bsa.mask_compile(kind, S, S, dense=dd, orientation=orientation, **kw)
+    host = {k: v.cpu().numpy() for k, v in info.arrays().items() if k in ("row_len", "row_order")}
+    info.destroy()
+    want_len = (ref.labels_unshrunk != 0).sum(axis=-1).reshape(-1)
+    assert np.array_equal(host["row_len"], want_len)
+    assert np.array_equal(host["row_order"], np.argsort(-want_len, kind="stable"))
