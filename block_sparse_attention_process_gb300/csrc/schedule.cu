@@ -145,6 +145,9 @@ bsa_status schedule_lists(const int32_t* row_len, const int32_t* row_order, int3
     }
     const int64_t greedy_max = *std::max_element(gload.begin(), gload.end());
     int64_t lo = std::max(biggest, (total + grid - 1) / grid), hi = greedy_max - 1;
+    // no assignment goes below lo: when even that is not 3% under the
+    // greedy's maximum, skip the search (many tiles per CTA)
+    if (100 * (greedy_max - lo) < 3 * greedy_max) hi = lo - 1;
     std::vector<int32_t> ff_owner(tiles.size()), best_owner;
     int64_t best_max = greedy_max;
     while (lo <= hi) {
