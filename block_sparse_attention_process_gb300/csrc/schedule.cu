@@ -214,6 +214,7 @@ bsa_status cached_schedule_lists(const bsa_mask_info* info, int32_t n_b, int32_t
   const bsa_status ls = schedule_lists(info->row_len_h.data(), info->row_order_h.data(), info->rows, info->heads, n_b,
                                        n_g, group, splits, grid, flat, stride);
   if (ls != BSA_OK) return ls;
+  if (flat->size() * sizeof(int4) > (size_t(4) << 20)) return BSA_OK;  // (not kept: over 4 MiB)
   ListsEntry e;
   e.row_len.assign(info->row_len_h.begin(), info->row_len_h.begin() + static_cast<std::ptrdiff_t>(n));
   e.row_order.assign(info->row_order_h.begin(), info->row_order_h.begin() + static_cast<std::ptrdiff_t>(n));
