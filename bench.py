@@ -397,6 +397,8 @@ def run_gpu(args):
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": round(step_ms, 4),
+            "step_ms_spread": {"min": round(min(step_times), 4), "median": round(statistics.median(step_times), 4),
+                               "max": round(max(step_times), 4)},
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
