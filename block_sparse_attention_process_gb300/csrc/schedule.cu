@@ -5,22 +5,21 @@
 // blocks costs 8n + 12 (in eighths of a block: about one and a half blocks
 // of per-tile work).  Two assignments are built: the greedy one (each tile,
 // longest first, to the CTA with the least work so far) and MULTIFIT
-// (Coffman, Garey and Johnson,
-// "An application of bin-packing to multiprocessor scheduling", 1978): the
-// smallest CTA capacity, found by bisection, under which first-fit
-// decreasing places every tile.  The greedy one is kept unless MULTIFIT's
-// maximum is at least 3% lower: its waves of similar tiles (the same rows of
-// the heads of a KV group at the same time) share K/V and Q/dO through L2,
-// and with many tiles per CTA it balances within about 1%.  With few tiles
-// per CTA and a few sizes repeated (the dK/dV tiles of a causal mask: every
-// key block once per KV head) it leaves the busiest CTAs ~7% above the
-// mean, and MULTIFIT ~0.4%.  Each CTA walks its
-// tiles longest first, so concurrently running CTAs work on tiles of similar
-// rows (and share their K/V and Q/dO blocks through L2).  Built schedules
-// are kept per (row lengths, row order, configuration) for the process, so a
-// mask compiled again (every training step) finds its schedule built.
+// (Coffman, Garey and Johnson, "An application of bin-packing to
+// multiprocessor scheduling", 1978): the smallest CTA capacity, found by
+// bisection, under which first-fit decreasing places every tile.  The
+// greedy one is kept unless MULTIFIT's maximum is at least 3% lower: its
+// waves of similar tiles (the same rows of the heads of a KV group at the
+// same time) share K/V and Q/dO through L2, and with many tiles per CTA it
+// balances within about 1%.  With few tiles per CTA and a few sizes
+// repeated (the dK/dV tiles of a causal mask: every key block once per KV
+// head) it leaves the busiest CTAs ~7% above the mean, and MULTIFIT ~0.4%.
+// Each CTA walks its tiles longest first.  Built schedules are kept per
+// (row lengths, row order, configuration) for the process, so a mask
+// compiled again (every training step) finds its schedule built.
 #include <algorithm>
 #include <cstddef>
+#include <cstdint>
 #include <iterator>
 #include <list>
 #include <mutex>
