@@ -181,6 +181,22 @@ bsa_status schedule_lists(const int32_t* row_len, const int32_t* row_order, int3
 
 namespace {
 
+// A piece of a tile schedule carried in a kernel's parameters (a launch
+// takes up to 32,764 bytes of them).  The launch path brings it to the
+// device, not a copy engine, so the upload does not wait behind large
+// host<->device copies that other streams have in flight (a pageable copy
+// of more than 64 KiB does, holding the calling thread until they end).
+constexpr int kPutInt4s = 1900;
+struct PutChunk {
+  int4 v[kPutInt4s];
+  int32_t n;
+};
+
+__global__ void __launch_bounds__(256) put_int4s(int4* __restrict__ dst, const __grid_constant__ PutChunk c) {
+  for (int i = threadIdx.x; i < c.n; i += blockDim.x) dst[i] = c.v[i];
+  __threadfence();
+}
+
 // Built schedules of the process, most recently used first: the host side
 // of a schedule depends only on the row lengths, the row order and the
 // launch configuration, which a mask compiled again repeats.
@@ -255,14 +271,25 @@ bsa_status tile_schedule(const bsa_mask_info* info, int32_t n_b, int32_t n_g, in
     if (ls != BSA_OK) return ls;
   }
   // stream-ordered upload (no synchronisation with earlier work on the
-  // device), from a host copy that lives as long as the schedule
+  // device) in kernel parameters; the host copy lives as long as the schedule
   bsa_mask_info::Schedule sc;
   sc.host = std::move(flat);
   void* dv = nullptr;
   bsa_status bs = pool_alloc(&dv, sc.host.size() * sizeof(int4), stream);
   if (bs != BSA_OK) return bs;
   int4* d = static_cast<int4*>(dv);
-  e = cudaMemcpyAsync(d, sc.host.data(), sc.host.size() * sizeof(int4), cudaMemcpyHostToDevice, stream);
+  e = cudaSuccess;
+  for (size_t off = 0; e == cudaSuccess && off < sc.host.size(); off += kPutInt4s) {
+    PutChunk c;
+    c.n = static_cast<int32_t>(std::min<size_t>(kPutInt4s, sc.host.size() - off));
+    std::copy(sc.host.begin() + static_cast<std::ptrdiff_t>(off),
+              sc.host.begin() + static_cast<std::ptrdiff_t>(off) + c.n, c.v);
+    put_int4s<<<1, 256, 0, stream>>>(d + off, c);
+    e = cudaGetLastError();
+  }
+  // (the event between the upload and the launch that reads the schedule
+  // also orders them fully: that launch's early start covers only its own
+  // predecessor kernel, and the forward's walker reads the schedule at once)
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sc.ready, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventRecord(sc.ready, stream);
   if (e != cudaSuccess) {
