@@ -180,9 +180,12 @@ typedef struct {
  * previous kernel on `stream`, and it waits for that kernel before reading
  * Q/K/V or writing O/LSE (BSA_PDL=0 in the environment turns this off).
  * The first launch of a (B, Hq, SM count) configuration builds its tile
- * schedule on the host and uploads it in stream order on `stream` (cached
- * in the MaskInfo; a later launch on another stream waits for the upload
- * through an event). */
+ * schedule on the host (kept for the process per row lengths and
+ * configuration, so a mask compiled again reuses it) and uploads it in
+ * stream order on `stream`, in the parameters of small copy kernels rather
+ * than through a copy engine, so that it never waits behind other streams'
+ * host<->device copies (cached in the MaskInfo; a later launch on another
+ * stream waits for the upload through an event). */
 BSA_API bsa_status bsa_fwd(const bsa_fwd_args* args, const bsa_mask_info* fwd_info, bsa_stream stream);
 
 /* One shard of the key axis ("Splash Attention: When the Mask Stops Being
